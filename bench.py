@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 exact-attention path; prints ONE JSON line (rank 0).
+
+A step is one fa_fwd call (the whole prefill path: tile scheduling, TMA loads,
+S = QK^T, masking, online softmax, lazy O correction, P V, epilogue) over the
+headline workload, the causal MHA prefill B=2, H=16, N=M=2048, d=128, bf16;
+inputs are resident in HBM and L2 is flushed (a 256 MiB write) between steps.
+Each step is timed with CUDA events on the launching stream.  The line also
+carries:
+  roofline      the prefill kernel against the measured dense bf16 peak;
+  e2e           the same metric through the public API with pinned host
+                buffers, host->device inputs and device->host O/LSE inside the
+                timed region;
+  decode        split-KV decode (B=2, H=8, M=65536, d=128, chunk 128) in HBM
+                GB/s against the measured copy bandwidth;
+  workloads     every workload's time and roofline fraction;
+  cpu_baseline  the fp64 CPU oracle, as it stands, on a bounded sample;
+  clocks        nvidia-smi samples taken during the timed regions.
+
+--impl reference times the oracle (the only other implementation of the
+method here) on the host cores, same metric and workload, a bounded sample per
+step.  With --gpus N > 1 (torchrun, one process per GPU) every rank runs its
+own replica of the workload (independent problems, no collective on the data
+path): value = N * work / max-over-ranks time, scaling "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("fwd attention TFLOPS (4·B·H·N·M·d, causal halved) and decode "
+          "HBM GB/s, % roofline")
+HEADLINE = "prefill_causal_b2_h16_n2048_bf16"
+DECODE = "decode_b2_h8_m65536_f16"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# process group (torchrun) helpers -- host logic, testable with gloo on CPU
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest value any rank holds (the job's time is its slowest rank's)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, traffic
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if absent or
+    taken on a different version of the kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    digest = kernel_source_digest()
+    for line in lines:
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload \
+                and parts[1] == kernel and parts[2] == digest:
+            return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.3)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.flush()
+        return False
+
+    def summary(self):
+        try:
+            with open(self.out.name) as f:
+                rows = [r.split(",") for r in f.read().splitlines() if r.strip()]
+            os.unlink(self.out.name)
+        except OSError:
+            rows = []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
+        for r in rows:
+            try:
+                vals = [x.strip() for x in r]
+                samples.append((float(vals[1]), float(vals[2]), float(vals[3]), float(vals[4]),
+                                vals[5:9]))
+            except (ValueError, IndexError):
+                continue
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [s for s in samples if s[3] >= 50.0] or samples
+        reasons = sorted({names[i] for s in loaded for i, v in enumerate(s[4])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(s[0] for s in loaded),
+                "sm_max_mhz": max(s[1] for s in samples),
+                "power_w_max": max(s[2] for s in samples),
+                "reasons": reasons, "samples": len(samples), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------------------
+# GPU timing
+# ---------------------------------------------------------------------------
+
+def time_calls(torch, fn, steps, warmup, flush=None, dist=None):
+    """Per-call device times (ms) with CUDA events on the current stream; the
+    optional flush runs between calls, outside the event pairs."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s, e in ev:
+        if flush is not None:
+            flush()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def bench_prefill(torch, fa, w, steps, warmup, flush, dist=None):
+    from exact_attention_05_gb300.workloads import workload_inputs
+    q, k, v = (t.cuda() for t in workload_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+
+    def call():
+        fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.M, w.d, int(w.causal), w.scale,
+                  w.dtype)
+
+    times = time_calls(torch, call, steps, warmup, flush, dist)
+    if fa.fa_get_last_device_status() != fa.FA_OK:
+        raise RuntimeError(f"{w.name}: a device-side wait expired")
+    return times
+
+
+def bench_decode(torch, fa, w, steps, warmup, flush, dist=None):
+    from exact_attention_05_gb300.workloads import workload_inputs
+    q, k, v = (t.cuda() for t in workload_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+
+    def call():
+        fa.fa_decode(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.M, w.d, w.chunk, w.scale, w.dtype)
+
+    times = time_calls(torch, call, steps, warmup, flush, dist)
+    if fa.fa_get_last_device_status() != fa.FA_OK:
+        raise RuntimeError(f"{w.name}: a device-side wait expired")
+    return times
+
+
+def bench_e2e_prefill(torch, fa, w, steps, warmup):
+    """Public API with pinned host buffers: H2D of q/k/v, fa_fwd, D2H of o/lse."""
+    from exact_attention_05_gb300.workloads import workload_inputs
+    qh, kh, vh = (t.pin_memory() for t in workload_inputs(w))
+    qd, kd, vd = torch.empty_like(qh, device="cuda"), torch.empty_like(kh, device="cuda"), \
+        torch.empty_like(vh, device="cuda")
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+    oh = torch.empty_like(qh).pin_memory()
+    lseh = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32).pin_memory()
+
+    def call():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        fa.fa_fwd(qd, kd, vd, od, lsed, w.B, w.Hq, w.Hkv, w.N, w.M, w.d, int(w.causal), w.scale,
+                  w.dtype)
+        oh.copy_(od, non_blocking=True)
+        lseh.copy_(lsed, non_blocking=True)
+
+    times = time_calls(torch, call, steps, warmup)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lseh.numel() * lseh.element_size()
+    return times, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, heads: int):
+    """A bounded sample of workload w for the oracle: batch 0, the first `heads`
+    query heads (with their kv heads), every query row.  Returns a callable that
+    runs it and the sample's algorithmic FLOPs."""
+    import oracle
+    from exact_attention_05_gb300.workloads import bits, workload_inputs
+    q, k, v = workload_inputs(w)
+    g = w.Hq // w.Hkv
+    kvh = -(-heads // g)
+    qs = bits(q[:1, :, :heads].contiguous())
+    ks = bits(k[:1, :, :kvh].contiguous())
+    vs = bits(v[:1, :, :kvh].contiguous())
+    if heads % g:
+        raise ValueError("sample must cover whole GQA groups")
+    flops = w.flops / (w.B * w.Hq) * heads
+
+    def run():
+        oracle.attention(qs, ks, vs, w.dtype, w.causal, w.scale)
+
+    return run, flops
+
+
+def cpu_baseline(w, target_s: float = 12.0):
+    import oracle
+    oracle.build()
+    g = w.Hq // w.Hkv
+    run, flops = oracle_sample(w, g)
+    t0 = time.perf_counter()
+    run()
+    t1 = time.perf_counter() - t0
+    groups = max(1, min(w.Hq // g, int(target_s / max(t1, 1e-6))))
+    heads = groups * g
+    if heads > g:
+        run, flops = oracle_sample(w, heads)
+        t0 = time.perf_counter()
+        run()
+        t1 = time.perf_counter() - t0
+    return {"value": flops / t1 / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"batch 0, query heads 0..{heads - 1} of {w.Hq} (all {w.N} rows), fp64, "
+                      f"{t1:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the oracle as it stands on the host cores."""
+    if rank != 0:
+        return 0
+    import oracle
+    from exact_attention_05_gb300.workloads import WORKLOADS, DTYPE_NAME
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    g = w.Hq // w.Hkv
+    run, flops = oracle_sample(w, g)
+    for _ in range(max(0, args.warmup)):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    mean_s = sum(times) / len(times)
+    value = flops / mean_s / 1e12
+    sample = f"batch 0, query heads 0..{g - 1} of {w.Hq} (all {w.N} rows) per step, fp64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": mean_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    from exact_attention_05_gb300.workloads import DTYPE_NAME
+    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "M": w.M, "d": w.d,
+           "dtype": DTYPE_NAME[w.dtype], "causal": w.causal, "scale": w.scale}
+    if w.kind == "decode":
+        cfg["chunk"] = w.chunk
+    if w.peaky_frac:
+        cfg["peaky_k_rows"] = w.peaky_frac
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-workload table, decode line and CPU baseline")
+    args = ap.parse_args(argv)
+    rank, local, world = dist_env()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import exact_attention_05_gb300 as fa
+    from exact_attention_05_gb300 import build as fa_build
+    from exact_attention_05_gb300.workloads import WORKLOADS
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(fa_build.LIB_PATH):
+        fa_build.build()
+    barrier(dist)
+    fa.load_library()
+    peaks, peak_src = load_peaks()
+    w = WORKLOADS[args.workload]
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_ctr = [0]
+
+    def flush():
+        flush_ctr[0] = (flush_ctr[0] + 1) & 0xFF
+        flush_buf.fill_(flush_ctr[0])
+
+    extras = {}
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        times = bench_prefill(torch, fa, w, args.steps, args.warmup, flush, dist)
+        mean_ms = sum(times) / len(times)
+        mean_ms_max = max_over_ranks(mean_ms, dist, device="cuda")
+        value = aggregate_throughput(w.flops, world, mean_ms_max * 1e-3) / 1e12
+
+        e2e_steps = max(3, min(args.steps, 20))
+        e2e_times, h2d, d2h = bench_e2e_prefill(torch, fa, w, e2e_steps, 3)
+        e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), dist, device="cuda")
+        e2e_value = aggregate_throughput(w.flops, world, e2e_ms * 1e-3) / 1e12
+
+        if not args.no_extras:
+            wd = WORKLOADS[DECODE]
+            dt = bench_decode(torch, fa, wd, max(3, min(args.steps, 50)), 3, None, dist)
+            d_ms = max_over_ranks(sum(dt) / len(dt), dist, device="cuda")
+            d_gbs = wd.decode_bytes / (d_ms * 1e-3) / 1e9
+            extras["decode"] = {
+                "workload": wd.name, "ms_per_call": d_ms, "value": d_gbs * world,
+                "unit": "GB/s", "launches_per_call": 2,
+                "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": d_gbs / peaks["hbm_gbs"],
+                             "traffic": recorded_traffic(wd.name, "decode_chunk_kernel"),
+                             "peak_source": peak_src,
+                             "note": "achieved over the whole call (chunk + merge kernels)"},
+            }
+            table = {}
+            for name, wl in WORKLOADS.items():
+                n = max(3, min(args.steps, 20 if wl.flops < 1e12 else 5))
+                if wl.kind == "prefill":
+                    tt = bench_prefill(torch, fa, wl, n, 3, flush if wl.flops < 1e12 else None,
+                                       dist)
+                    ms = max_over_ranks(statistics.median(tt), dist, device="cuda")
+                    tf = wl.flops / (ms * 1e-3) / 1e12
+                    table[name] = {"ms": ms, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}
+                else:
+                    tt = bench_decode(torch, fa, wl, n, 3, flush, dist)
+                    ms = max_over_ranks(statistics.median(tt), dist, device="cuda")
+                    gbs = wl.decode_bytes / (ms * 1e-3) / 1e9
+                    table[name] = {"ms": ms, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+            extras["workloads"] = table
+    clk = clocks.summary()
+
+    if rank == 0 and world == 1 and not args.no_extras:
+        try:
+            extras["cpu_baseline"] = cpu_baseline(w)
+        except Exception as exc:  # the CPU leg never decides the GPU numbers
+            extras["cpu_baseline"] = {"value": None, "unit": "TFLOP/s", "cores": None,
+                                      "kind": "oracle", "sample": f"failed: {exc}"}
+
+    achieved = w.flops / (mean_ms_max * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": mean_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(workload_config(w), l2="flushed between steps (256 MiB write)",
+                       parallelism=f"replicas x{world}"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(w.name, "prefill_kernel"),
+                     "peak_source": f"{peak_src} dense bf16 burst"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    line.update(extras)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

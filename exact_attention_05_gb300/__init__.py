@@ -1,0 +1,185 @@
+"""Thin Python binding of libfa.so, the GB300 exact-attention C ABI (include/fa.h).
+
+Only argument marshalling happens here: every step of the attention runs in the
+library's CUDA kernels.  PyTorch is used for device memory and streams.  There
+is no fallback: if the library is not built, every call raises.
+
+The functions mirror the C entry points one to one (``fa_fwd``, ``fa_decode``,
+``fa_status_string``, ``fa_get_last_device_status``, ...); pointer arguments
+accept a torch tensor (its ``data_ptr()``), an int address, or None, and the
+stream argument accepts a ``torch.cuda.Stream``, an int handle, or None for
+torch's current stream.  ``attention_forward`` and ``decode`` are shape-checked
+conveniences that allocate the outputs and call the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from .workloads import BF16, FP16
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libfa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_NO_MEMORY = 4
+FA_ERR_TIMEOUT = 5
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} ({status})")
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/fa.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def load_library():
+    """Loads libfa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with exact_attention_05_gb300.build.build() "
+                "(the attention path has no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, fp, I, F = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, I, F, I, vp]
+        lib.fa_fwd.restype = I
+        lib.fa_decode.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
+        lib.fa_decode.restype = I
+        lib.fa_status_string.argtypes = [I]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_get_last_device_status.argtypes = [vp]
+        lib.fa_get_last_device_status.restype = I
+        lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_set_wait_timeout_ns.restype = None
+        lib.fa_selftest_wait_timeout.argtypes = [vp]
+        lib.fa_selftest_wait_timeout.restype = I
+        lib.fa_release_workspaces.argtypes = []
+        lib.fa_release_workspaces.restype = None
+        lib.fa_abi_version.argtypes = []
+        lib.fa_abi_version.restype = I
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str) -> int:
+    if status != FA_OK:
+        raise FAError(status, where)
+    return status
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, M, d, causal, scale, dtype, stream=None,
+           check=True) -> int:
+    st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                               int(Hkv), int(N), int(M), int(d), int(causal), float(scale),
+                               int(dtype), _stream(stream))
+    return _check(st, "fa_fwd") if check else st
+
+
+def fa_decode(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, stream=None,
+              check=True) -> int:
+    st = load_library().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                                  int(Hkv), int(M), int(d), int(chunk), float(scale), int(dtype),
+                                  _stream(stream))
+    return _check(st, "fa_decode") if check else st
+
+
+def fa_get_last_device_status(stream=None) -> int:
+    return load_library().fa_get_last_device_status(_stream(stream))
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    load_library().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_selftest_wait_timeout(stream=None) -> int:
+    return load_library().fa_selftest_wait_timeout(_stream(stream))
+
+
+def fa_release_workspaces() -> None:
+    load_library().fa_release_workspaces()
+
+
+def fa_abi_version() -> int:
+    return load_library().fa_abi_version()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FP16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: fp16 or bf16")
+
+
+def attention_forward(q, k, v, causal: bool, scale: float, out=None, lse=None, with_lse=True,
+                      stream=None):
+    """O (and LSE) of q [B,N,Hq,d] against k/v [B,M,Hkv,d], all contiguous CUDA tensors."""
+    import torch
+    B, N, Hq, d = q.shape
+    _, M, Hkv, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    for t in (q, k, v, out):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    fa_fwd(q, k, v, out, lse, B, Hq, Hkv, N, M, d, int(bool(causal)), scale, _dtype_code(q),
+           stream)
+    return out, lse
+
+
+def decode(q, k, v, chunk: int, scale: float, out=None, lse=None, with_lse=True, stream=None):
+    """Split-KV decode of q [B,1,Hq,d] against k/v [B,M,Hkv,d]."""
+    import torch
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes q of shape [B, 1, Hq, d]")
+    _, M, Hkv, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    fa_decode(q, k, v, out, lse, B, Hq, Hkv, M, d, chunk, scale, _dtype_code(q), stream)
+    return out, lse

@@ -1,0 +1,266 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument
+// checks (all of them before any CUDA call), per-device state (architecture
+// check, device status word, decode workspaces), TMA tensor-map encoding and
+// the kernel launches.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+#define FA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+
+struct DeviceState {
+    bool checked = false;
+    bool supported = false;
+    int* status = nullptr;
+    std::map<cudaStream_t, Workspace> workspaces;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+constexpr uint64_t kMaxElements = 1ull << 39;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Pure argument checks shared by both operations; no CUDA call.
+fa_status check_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     int B, int Hq, int Hkv, int N, int M, int d, float scale, int dtype) {
+    if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || M <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return FA_ERR_INVALID_ARG;
+    if (lse && !aligned(lse, 4)) return FA_ERR_INVALID_ARG;
+    if ((uint64_t)B * N * Hq * d >= kMaxElements) return FA_ERR_INVALID_ARG;
+    if ((uint64_t)B * M * Hkv * d >= kMaxElements) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+// Current device's state; checks the architecture once and creates the status word.
+fa_status device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_devices[dev];
+    if (!st.checked) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        st.supported = (major == 10 && minor == 3);
+        if (st.supported) {
+            if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return FA_ERR_NO_MEMORY;
+            if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess ||
+                cudaDeviceSynchronize() != cudaSuccess)
+                return FA_ERR_CUDA;
+        }
+        st.checked = true;
+    }
+    if (!st.supported) return FA_ERR_UNSUPPORTED;
+    if (g_encode == nullptr) {
+        cudaDriverEntryPointQueryResult q{};
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = &st;
+    return FA_OK;
+}
+
+// 4-D map over a [batch, seq, heads, d] tensor: dims innermost first
+// {d, heads, seq, batch}; the box is box_d x 1 x box_rows x 1.
+fa_status encode_map(CUtensorMap* map, const void* base, int dtype, int d, int heads, int seq,
+                     int batch, int box_d, int box_rows, bool swizzle128) {
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)seq,
+                                (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2,
+                                   (cuuint64_t)seq * heads * d * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = g_encode(
+        map, dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+        4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Workspace of at least `bytes` for (device, stream).
+fa_status workspace(DeviceState* st, cudaStream_t stream, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace& w = st->workspaces[stream];
+    if (w.bytes < bytes) {
+        if (w.ptr != nullptr) {
+            // the old buffer may still be read by work in flight on this stream
+            if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        size_t want = bytes + bytes / 4;
+        want = (want + (1u << 20) - 1) & ~size_t((1u << 20) - 1);
+        if (cudaMalloc(&w.ptr, want) != cudaSuccess) {
+            (void)cudaGetLastError();
+            w.ptr = nullptr;
+            return FA_ERR_NO_MEMORY;
+        }
+        w.bytes = want;
+    }
+    *out = w.ptr;
+    return FA_OK;
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+FA_EXPORT fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                           int Hq, int Hkv, int N, int M, int d, int causal, float scale,
+                           fa_dtype dtype, fa_stream_t stream) {
+    fa_status s = check_args(q, k, v, o, lse, B, Hq, Hkv, N, M, d, scale, (int)dtype);
+    if (s != FA_OK) return s;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    const long long n_qtiles = (N + fa::kPrefillTile - 1) / fa::kPrefillTile;
+    if (n_qtiles * B * Hq > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != FA_OK) return s;
+    CUtensorMap tq, tk, tv, to;
+    if ((s = encode_map(&tq, q, dtype, d, Hq, N, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
+    if ((s = encode_map(&tk, k, dtype, d, Hkv, M, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
+    if ((s = encode_map(&tv, v, dtype, d, Hkv, M, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
+    if ((s = encode_map(&to, o, dtype, d, Hq, N, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
+    fa::PrefillArgs a{};
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.M = M;
+    a.causal = causal;
+    a.n_qtiles = (int)n_qtiles;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.lse = lse;
+    a.status = st->status;
+    a.timeout_ns = g_timeout_ns.load();
+    return from_cuda(fa::launch_prefill(tq, tk, tv, to, a, d, (int)dtype, (cudaStream_t)stream));
+}
+
+FA_EXPORT fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int M, int d, int chunk, float scale,
+                              fa_dtype dtype, fa_stream_t stream) {
+    fa_status s = check_args(q, k, v, o, lse, B, Hq, Hkv, 1, M, d, scale, (int)dtype);
+    if (s != FA_OK) return s;
+    if (chunk <= 0) return FA_ERR_INVALID_ARG;
+    if ((long long)B * Hkv > 65535) return FA_ERR_INVALID_ARG;
+    const int nc = (int)(((long long)M + chunk - 1) / chunk);
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != FA_OK) return s;
+    const size_t part_elems = (size_t)B * Hq * nc * d;
+    const size_t bytes = (part_elems + (size_t)B * Hq * nc) * sizeof(float);
+    void* ws = nullptr;
+    if ((s = workspace(st, (cudaStream_t)stream, bytes, &ws)) != FA_OK) return s;
+    CUtensorMap tk, tv;
+    if ((s = encode_map(&tk, k, dtype, d, Hkv, M, B, d, fa::kDecodeSubTile, false)) != FA_OK) return s;
+    if ((s = encode_map(&tv, v, dtype, d, Hkv, M, B, d, fa::kDecodeSubTile, false)) != FA_OK) return s;
+    fa::DecodeArgs a{};
+    a.q = q;
+    a.o = o;
+    a.lse = lse;
+    a.o_part = static_cast<float*>(ws);
+    a.lse_part = static_cast<float*>(ws) + part_elems;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.M = M;
+    a.chunk = chunk;
+    a.nc = nc;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.status = st->status;
+    a.timeout_ns = g_timeout_ns.load();
+    return from_cuda(fa::launch_decode(tk, tv, a, d, (int)dtype, (cudaStream_t)stream));
+}
+
+FA_EXPORT const char* fa_status_string(fa_status status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dim, dtype or device";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or launch failed";
+        case FA_ERR_NO_MEMORY: return "FA_ERR_NO_MEMORY: workspace allocation failed";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait expired";
+    }
+    return "unknown fa_status";
+}
+
+FA_EXPORT fa_status fa_get_last_device_status(fa_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceState* st = nullptr;
+    const fa_status s = device_state(&st);
+    if (s != FA_OK) return s == FA_ERR_UNSUPPORTED ? FA_OK : s;
+    int word = 0;
+    if (cudaMemcpy(&word, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (word == 0) return FA_OK;
+    if (cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return FA_ERR_CUDA;
+    return (word & 0xff) == FA_DEV_TIMEOUT ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+}
+
+FA_EXPORT void fa_set_wait_timeout_ns(unsigned long long ns) {
+    g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
+}
+
+FA_EXPORT fa_status fa_selftest_wait_timeout(fa_stream_t stream) {
+    DeviceState* st = nullptr;
+    const fa_status s = device_state(&st);
+    if (s != FA_OK) return s;
+    return from_cuda(fa::launch_wait_selftest(st->status, g_timeout_ns.load(), (cudaStream_t)stream));
+}
+
+FA_EXPORT void fa_release_workspaces(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    for (auto& kv : g_devices) {
+        if (kv.second.workspaces.empty()) continue;
+        if (cudaSetDevice(kv.first) != cudaSuccess) continue;
+        cudaDeviceSynchronize();
+        for (auto& w : kv.second.workspaces)
+            if (w.second.ptr) cudaFree(w.second.ptr);
+        kv.second.workspaces.clear();
+    }
+    if (have_cur) cudaSetDevice(cur);
+}
+
+FA_EXPORT int fa_abi_version(void) { return 1; }

@@ -1,0 +1,64 @@
+// fa_internal.h -- declarations shared by the translation units of libfa.so
+// (host launchers and the argument blocks the kernels receive).  Not part of
+// the public ABI; include/fa.h is.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+// Low byte of the device status word; the next byte says which wait expired.
+#define FA_DEV_TIMEOUT 1
+
+// Where a bounded wait sits (recorded in bits 8.. of the status word).
+enum FaWaitSite {
+    FA_SITE_PRODUCER_SLOT = 1,
+    FA_SITE_MMA_Q = 2,
+    FA_SITE_MMA_KV = 3,
+    FA_SITE_MMA_P = 4,
+    FA_SITE_SOFTMAX_S = 5,
+    FA_SITE_SOFTMAX_O = 6,
+    FA_SITE_DRAIN = 7,
+    FA_SITE_DECODE_KV = 8,
+    FA_SITE_SELFTEST = 9,
+};
+
+namespace fa {
+
+struct PrefillArgs {
+    int B, Hq, Hkv, N, M;
+    int causal;
+    int n_qtiles;          // ceil(N / 128)
+    float scale_log2;      // scale * log2(e)
+    float* lse;            // [B, Hq, N] or nullptr
+    int* status;           // device status word
+    unsigned long long timeout_ns;
+};
+
+struct DecodeArgs {
+    const void* q;         // [B, 1, Hq, d]
+    void* o;               // [B, 1, Hq, d]
+    float* lse;            // [B, Hq] or nullptr
+    float* o_part;         // workspace [B, Hq, nc, d] fp32
+    float* lse_part;       // workspace [B, Hq, nc] fp32, log2 domain
+    int B, Hq, Hkv, M, chunk, nc;
+    float scale_log2;
+    int* status;
+    unsigned long long timeout_ns;
+};
+
+// dtype: 0 = fp16, 1 = bf16; d in {64, 128}.
+cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& to, const PrefillArgs& a, int d, int dtype,
+                           cudaStream_t stream);
+
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int d,
+                          int dtype, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cudaStream_t stream);
+
+// Geometry the host needs to build tensor maps.
+constexpr int kPrefillTile = 128;   // query rows per tile and keys per KV tile
+constexpr int kDecodeSubTile = 128; // keys per decode sub-tile
+
+}  // namespace fa

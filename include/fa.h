@@ -1,0 +1,147 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library, libfa.so.
+ *
+ * Two operations, both the exact attention O = softmax(scale * Q K^T [+ mask]) V
+ * computed with an online softmax so that S and P never reach HBM:
+ *
+ *   fa_fwd     prefill / forward.  Q is cut into tiles of query rows, K/V are
+ *              streamed in tiles while a running max m and sum l are kept and
+ *              the normalisation is deferred to the end ("[CUDA 优化实战] fmha
+ *              sm120 : 超越 torch.sdpa(flash-attention-2)", section 1 "flash
+ *              attention" and section 2 "fmha 实现"), with GQA, an optional
+ *              top-left causal mask and a per-row log-sum-exp output.
+ *
+ *   fa_decode  split-KV flash decoding for a single query row per head: the M
+ *              keys are cut into chunks, each chunk yields a partial O_c
+ *              (normalised inside the chunk) and lse_c, and an LSE-weighted
+ *              merge combines them ("CUDA 实现 Flash Decoding：解码阶段并行度重建
+ *              与性能剖析", section 2.2 Steps 1 and 2, section 3 "两段式 kernel").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layouts are contiguous, heads inner: q and o [B, N, Hq, d]; k and v
+ *    [B, M, Hkv, d]; lse [B, Hq, N] fp32.  Decode uses N = 1: q/o [B, 1, Hq, d],
+ *    lse [B, Hq].
+ *  - Element type: fp16 or bf16 for q, k, v and o (all four the same); all
+ *    arithmetic accumulates in fp32.  o is rounded to nearest-even.
+ *  - GQA: query head h reads kv head h / (Hq / Hkv); Hq % Hkv must be 0.
+ *  - Causal (fa_fwd only): key j is visible to query i iff j <= i (top-left
+ *    aligned, so no row is ever empty).
+ *  - lse is the natural log of sum_j exp(scale * q_i . k_j) over the visible
+ *    keys, in fp32 ("Tensor Core 迁移计划", cross-cutting concerns: the LSE
+ *    output stays fp32).  lse may be NULL; it is then not written.
+ *  - Pointers are DEVICE pointers owned by the caller (the library never
+ *    allocates, frees or keeps them); q, k, v, o must be 16-byte aligned, lse
+ *    4-byte aligned.  The output buffers must not overlap the inputs.
+ *  - Calls are asynchronous on `stream` (NULL = legacy default stream) on the
+ *    current CUDA device, which must be compute capability 10.3 (GB300).
+ *  - The return value reports argument errors (checked before any CUDA call)
+ *    and launch errors; it does not synchronise.  Device-side failures of the
+ *    bounded waits are reported later by fa_get_last_device_status().
+ *  - Errors are return codes; nothing asserts or aborts the process.
+ */
+#ifndef FA_H
+#define FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+struct CUstream_st;
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+    FA_FP16 = 0,
+    FA_BF16 = 1
+} fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, Hq % Hkv != 0,
+                                 misaligned pointer, bad scale, size overflow */
+    FA_ERR_UNSUPPORTED = 2,   /* d not in {64, 128}, unknown dtype, device not sm_103 */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or kernel launch failed */
+    FA_ERR_NO_MEMORY = 4,     /* the decode workspace could not be allocated */
+    FA_ERR_TIMEOUT = 5        /* a device-side bounded wait expired (see below) */
+} fa_status;
+
+/*
+ * Exact attention forward (prefill).
+ *
+ *   q   [B, N, Hq, d]   fp16/bf16, device
+ *   k   [B, M, Hkv, d]  same type
+ *   v   [B, M, Hkv, d]  same type
+ *   o   [B, N, Hq, d]   same type, written
+ *   lse [B, Hq, N]      fp32, written unless NULL
+ *   causal  0 = full attention, 1 = top-left causal mask
+ *   scale   multiplies the logits; must be finite and > 0 (usually 1/sqrt(d))
+ *
+ * Limits: B, Hq, Hkv, N, M >= 1; d in {64, 128}; B*N*Hq*d and B*M*Hkv*d
+ * below 2^40 elements.  Returns FA_OK once the work is enqueued.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int N, int M, int d, int causal,
+                 float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Split-KV flash decoding (one query row per head).
+ *
+ *   q   [B, 1, Hq, d]   fp16/bf16, device
+ *   k   [B, M, Hkv, d]  same type
+ *   v   [B, M, Hkv, d]  same type
+ *   o   [B, 1, Hq, d]   same type, written
+ *   lse [B, Hq]         fp32, written unless NULL
+ *   chunk   keys per split (>= 1); the split count is nc = ceil(M / chunk),
+ *           the last chunk may be short.
+ *
+ * Two kernels run back to back on `stream`: the chunk kernel writes nc fp32
+ * partials (O_c, lse_c) per (b, h) into a workspace, the merge kernel combines
+ * them.  The workspace (B*Hq*nc*(d+1) fp32 values) is owned by the library:
+ * one buffer per (device, stream), allocated on first use, grown on demand
+ * (growing synchronises the device) and kept until fa_release_workspaces().
+ * Calls on the same stream are ordered by the stream; calls on different
+ * streams use different buffers.  FA_ERR_NO_MEMORY if it cannot be allocated.
+ */
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int Hq, int Hkv, int M, int d, int chunk,
+                    float scale, fa_dtype dtype, fa_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* fa_status_string(fa_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Every spin-wait inside the kernels is bounded; when one expires the
+ * kernel records FA_ERR_TIMEOUT there, drains its own in-flight copies and
+ * tensor-core work, frees its tensor memory and returns (its outputs are then
+ * undefined).  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+fa_status fa_get_last_device_status(fa_stream_t stream);
+
+/*
+ * Sets the limit of every device-side wait, in nanoseconds, for launches made
+ * after the call (process-wide; default 2e9 = 2 s; 0 restores the default).
+ */
+void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * Test hook for the bounded-wait path: launches one CTA that waits on a
+ * shared-memory barrier nobody arrives on, under the current wait limit, so
+ * that the wait expires and the kernel records FA_ERR_TIMEOUT in the status
+ * word.  It faults nothing and leaves the context usable.
+ */
+fa_status fa_selftest_wait_timeout(fa_stream_t stream);
+
+/* Frees every decode workspace the library holds (synchronises each device used). */
+void fa_release_workspaces(void);
+
+/* ABI version of this header, 1. */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */
