@@ -30,6 +30,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_NO_MEMORY = 4
 FA_ERR_TIMEOUT = 5
+FA_ERR_SCRATCH_LIMIT = 6
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +65,8 @@ def load_library():
         lib.fa_fwd.restype = I
         lib.fa_decode.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
         lib.fa_decode.restype = I
+        lib.fa_decode_noalloc.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
+        lib.fa_decode_noalloc.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_get_last_device_status.argtypes = [vp]
@@ -121,6 +124,16 @@ def fa_decode(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, stream=Non
                                   int(Hkv), int(M), int(d), int(chunk), float(scale), int(dtype),
                                   _stream(stream))
     return _check(st, "fa_decode") if check else st
+
+
+def fa_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, stream=None,
+                      check=True) -> int:
+    """fa_decode with its partials in the library's static device scratch: for
+    callers that cannot allocate device memory (no cudaMalloc is made)."""
+    st = load_library().fa_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                          int(Hq), int(Hkv), int(M), int(d), int(chunk),
+                                          float(scale), int(dtype), _stream(stream))
+    return _check(st, "fa_decode_noalloc") if check else st
 
 
 def fa_get_last_device_status(stream=None) -> int:

@@ -219,6 +219,8 @@ FA_EXPORT const char* fa_status_string(fa_status status) {
         case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or launch failed";
         case FA_ERR_NO_MEMORY: return "FA_ERR_NO_MEMORY: workspace allocation failed";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait expired";
+        case FA_ERR_SCRATCH_LIMIT:
+            return "FA_ERR_SCRATCH_LIMIT: the problem needs more than the static decode scratch";
     }
     return "unknown fa_status";
 }

@@ -63,7 +63,9 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,   /* d not in {64, 128}, unknown dtype, device not sm_103 */
     FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or kernel launch failed */
     FA_ERR_NO_MEMORY = 4,     /* the decode workspace could not be allocated */
-    FA_ERR_TIMEOUT = 5        /* a device-side bounded wait expired (see below) */
+    FA_ERR_TIMEOUT = 5,       /* a device-side bounded wait expired (see below) */
+    FA_ERR_SCRATCH_LIMIT = 6  /* the problem needs more than the static scratch of
+                                 fa_decode_noalloc holds */
 } fa_status;
 
 /*
@@ -106,6 +108,36 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int Hq, int Hkv, int M, int d, int chunk,
                     float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Split-KV decode that allocates no device memory.  The pages have no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- code running while a CUDA graph is captured, processes whose
+ * device memory must all come from their own pool, hosts that forbid
+ * allocation after start-up.
+ *
+ * Same arguments, layouts, results and argument errors as fa_decode, but the
+ * fp32 chunk partials live in one array of static device memory of
+ * FA_DECODE_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the
+ * library's module holds until the process exits.  A problem needing more
+ * than that -- B*Hq*ceil(M/chunk)*(d+1)*4 bytes -- returns
+ * FA_ERR_SCRATCH_LIMIT before any launch (B=2, Hq=8, M=65536, chunk=128,
+ * d=128 needs 4.2 MB).  The call makes no cudaMalloc, cudaFree or other
+ * allocating call.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current): make
+ * that first call before any stream capture starts.  All calls share the one
+ * array and it keeps the previous call's contents; nothing in it needs to
+ * start at zero, but calls that overlap on the GPU (e.g. on two streams with
+ * no ordering between them) race on it and give undefined results.  Device
+ * wait timeouts of these launches are recorded in a status word of their
+ * own, not the one fa_get_last_device_status() reads.
+ */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int M, int d, int chunk,
+                            float scale, fa_dtype dtype, fa_stream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(fa_status status);

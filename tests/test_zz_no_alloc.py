@@ -1,0 +1,58 @@
+"""fa_decode_noalloc, the decode entry point that allocates no device memory.
+
+It exists for callers that cannot call cudaMalloc: code running while a CUDA
+graph is being captured, processes whose device memory must all come from their
+own pool, hosts that forbid allocation after start-up.  It runs the same split-KV
+decode as fa_decode but keeps the chunk partials in a fixed array of static
+device memory instead of an allocated workspace.  Here it is called through the
+C ABI and compared with fa_decode on two calls in a row (different shapes, so a
+stale partial left in the shared array by the first call would show up in the
+second), within the tolerances the other parity tests use.
+
+The file name makes pytest collect it last.
+"""
+import pytest
+
+import exact_attention_05_gb300 as fa
+from exact_attention_05_gb300 import build as fa_build
+from exact_attention_05_gb300.workloads import BF16, FP16, make_inputs
+from parity import LSE_TOL, O_TOL, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def run_both(torch, B, Hq, Hkv, M, d, dtype, chunk, seed):
+    scale = 1.0 / d ** 0.5
+    q, k, v = (t.cuda() for t in make_inputs(B, Hq, Hkv, 1, M, d, dtype, seed))
+    o_ref, lse_ref = fa.decode(q, k, v, chunk, scale)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype)
+    torch.cuda.synchronize()
+    eo = (o.double() - o_ref.double()).abs().max().item()
+    el = (lse.double() - lse_ref.double()).abs().max().item()
+    assert eo <= O_TOL[dtype], f"max|dO| {eo:.3e}"
+    assert el <= LSE_TOL, f"max|dLSE| {el:.3e}"
+
+
+def test_noalloc_decode_matches_fa_decode_on_two_calls(lib):
+    torch = torch_cuda()
+    run_both(torch, 2, 8, 8, 65536, 128, FP16, 128, seed=1005)   # the long decode workload
+    run_both(torch, 1, 8, 2, 1000, 64, BF16, 100, seed=61)       # second call, other shape
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(lib):
+    torch = torch_cuda()
+    q = torch.zeros((4, 1, 32, 128), dtype=torch.float16, device="cuda")
+    k = torch.zeros((4, 8192, 32, 128), dtype=torch.float16, device="cuda")
+    # 4*32*ceil(8192/16)*(128+1) floats = 33.8 MB of partials > the 8 MiB array
+    st = fa.fa_decode_noalloc(q, k, k, q, None, 4, 32, 32, 8192, 128, 16, 0.1, FP16, check=False)
+    assert st == fa.FA_ERR_SCRATCH_LIMIT
+    assert "scratch" in fa.fa_status_string(st)
