@@ -38,10 +38,7 @@ struct DeviceState {
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using fa::EncodeTiledFn;
 EncodeTiledFn g_encode = nullptr;
 
 constexpr uint64_t kMaxElements = 1ull << 39;
@@ -191,8 +188,7 @@ FA_EXPORT fa_status fa_decode(const void* q, const void* k, const void* v, void*
     void* ws = nullptr;
     if ((s = workspace(st, (cudaStream_t)stream, bytes, &ws)) != FA_OK) return s;
     CUtensorMap tk, tv;
-    if ((s = encode_map(&tk, k, dtype, d, Hkv, M, B, d, fa::kDecodeSubTile, false)) != FA_OK) return s;
-    if ((s = encode_map(&tv, v, dtype, d, Hkv, M, B, d, fa::kDecodeSubTile, false)) != FA_OK) return s;
+    if (!fa::encode_decode_maps(g_encode, k, v, dtype, d, Hkv, M, B, &tk, &tv)) return FA_ERR_CUDA;
     fa::DecodeArgs a{};
     a.q = q;
     a.o = o;

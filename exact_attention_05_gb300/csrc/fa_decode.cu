@@ -40,40 +40,50 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D>
 struct DecodeCfg {
     static constexpr int TK = kDecodeSubTile;        // keys per sub-tile (TMA box rows)
-    static constexpr int THREADS = 128;
-    static constexpr int GMAX = 8;                   // query heads per pass over the tile
-    static constexpr int EPL = D / 32;               // elements of a key row per lane
-    static constexpr int KG = 128 / D;               // key groups in the P.V step
+    static constexpr int THREADS = 128;              // thread <-> key in the score step
+    static constexpr int GMAX = 4;                   // query heads per pass over the tile
+    static constexpr int NSUB = D / 64;              // 128-byte column halves of a K row
+    static constexpr int SUB_BYTES = TK * 128;       // one swizzled K half-tile
+    static constexpr int KQ = 256 / D;               // key groups in the P.V step
     static constexpr int TILE_BYTES = TK * D * 2;
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = TILE_BYTES;
-    static constexpr int SC_OFF = 2 * TILE_BYTES;                 // float [GMAX][TK]
-    static constexpr int RED_OFF = SC_OFF + GMAX * TK * 4;        // float [GMAX][KG][D]
-    static constexpr int HS_OFF = RED_OFF + GMAX * KG * D * 4;    // per head m, l, alpha
+    static constexpr int K_OFF = 0;                                // swizzled [NSUB][TK][64]
+    static constexpr int V_OFF = TILE_BYTES;                       // plain [TK][D]
+    static constexpr int QS_OFF = 2 * TILE_BYTES;                  // float [GMAX][D]
+    static constexpr int SC_OFF = QS_OFF + GMAX * D * 4;           // float [GMAX][TK]
+    static constexpr int RED_OFF = SC_OFF + GMAX * TK * 4;         // float2 [KQ-1][GMAX][D/2]
+    static constexpr int HS_OFF = RED_OFF + (KQ - 1) * GMAX * D * 4;  // per head m, l, alpha
     static constexpr int BAR_OFF = HS_OFF + 3 * GMAX * 4;
     static constexpr int MISC_OFF = BAR_OFF + 16;
-    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 128;        // + slack to align to 128 B
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;        // + slack to align to 1 KB
 };
 
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
+    const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y), c = unpack2<T>(w.z), d = unpack2<T>(w.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
 template <int D, typename T>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 3)
     decode_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
     using C = DecodeCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                               ~uintptr_t(127));
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
     const uint32_t kbar = sbase + C::BAR_OFF;
     const uint32_t vbar = kbar + 8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
+    float* qs = reinterpret_cast<float*>(smem + C::QS_OFF);
     float* sc = reinterpret_cast<float*>(smem + C::SC_OFF);
-    float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
+    float2* red = reinterpret_cast<float2*>(smem + C::RED_OFF);
     float* hm = reinterpret_cast<float*>(smem + C::HS_OFF);
     float* hl = hm + C::GMAX;
     float* halpha = hl + C::GMAX;
-    const T* Ks = reinterpret_cast<const T*>(smem + C::K_OFF);
-    const T* Vs = reinterpret_cast<const T*>(smem + C::V_OFF);
+    const uint8_t* Ks = smem + C::K_OFF;
+    const uint32_t* Vw = reinterpret_cast<const uint32_t*>(smem + C::V_OFF);  // pairs of T
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -97,82 +107,100 @@ __global__ void __launch_bounds__(128)
     __syncthreads();
     const WaitCtl wc{abort_flag, a.status, a.timeout_ns};
 
-    int loads = 0;  // sub-tiles loaded so far (phase of both barriers)
+    int loads = 0;  // sub-tiles loaded so far (the phase of both barriers)
     auto load_subtile = [&](int st) {
         if (tid == 0) {
+            const int row = key0 + st * C::TK;
             mbar_arrive_expect_tx(kbar, C::TILE_BYTES);
-            tma_load_4d(sbase + C::K_OFF, &tm_k, 0, kvh, key0 + st * C::TK, b, kbar);
+#pragma unroll
+            for (int s = 0; s < C::NSUB; ++s)
+                tma_load_4d(sbase + C::K_OFF + s * C::SUB_BYTES, &tm_k, s * 64, kvh, row, b, kbar);
             mbar_arrive_expect_tx(vbar, C::TILE_BYTES);
-            tma_load_4d(sbase + C::V_OFF, &tm_v, 0, kvh, key0 + st * C::TK, b, vbar);
+            tma_load_4d(sbase + C::V_OFF, &tm_v, 0, kvh, row, b, vbar);
         }
         ++loads;
     };
+    // The first sub-tile's copies go out before anything else.
+    load_subtile(0);
 
     bool ok = true;
-    const int col = tid % D;       // output column of this thread in the P.V step
-    const int kg = tid / D;        // its key group
+    // P.V mapping: thread <-> (column pair cp, key group kq)
+    constexpr int NCP = D / 2;
+    const int cp = tid % NCP;
+    const int kq = tid / NCP;
+    constexpr int KPG = C::TK / C::KQ;  // keys per group
     for (int hg = 0; hg < g && ok; hg += C::GMAX) {
         const int G = min(C::GMAX, g - hg);
-        // this pass's query heads, kept in fp32 registers: lane holds EPL elements
-        float qf[C::GMAX][C::EPL];
-#pragma unroll
-        for (int gi = 0; gi < C::GMAX; ++gi) {
+        // this pass's query heads, as fp32 in shared memory (read as broadcasts)
+        for (int e = tid; e < C::GMAX * D; e += C::THREADS) {
+            const int gi = e / D, col = e % D;
+            float val = 0.f;
             if (gi < G) {
                 const int h = kvh * g + hg + gi;
-                const T* qrow = reinterpret_cast<const T*>(a.q) + (size_t(b) * a.Hq + h) * D;
-#pragma unroll
-                for (int e = 0; e < C::EPL; e += 2) {
-                    const float2 f =
-                        unpack2<T>(*reinterpret_cast<const uint32_t*>(qrow + lane * C::EPL + e));
-                    qf[gi][e] = f.x;
-                    qf[gi][e + 1] = f.y;
-                }
+                val = static_cast<float>(
+                    reinterpret_cast<const T*>(a.q)[(size_t(b) * a.Hq + h) * D + col]);
             }
+            qs[e] = val;
         }
         if (tid < C::GMAX) {
             hm[tid] = -INFINITY;
             hl[tid] = 0.f;
         }
-        float acc[C::GMAX];
+        float2 acc[C::GMAX];
 #pragma unroll
-        for (int gi = 0; gi < C::GMAX; ++gi) acc[gi] = 0.f;
+        for (int gi = 0; gi < C::GMAX; ++gi) acc[gi] = make_float2(0.f, 0.f);
 
         for (int st = 0; st < nsub; ++st) {
             const int ks = key0 + st * C::TK;
             const int nk = min(C::TK, key1 - ks);
-            // the tile of a single-sub-tile chunk stays resident across head groups
-            const bool need_load = (hg == 0) || (nsub > 1);
-            if (need_load) load_subtile(st);
+            if (st > 0 || hg > 0) {
+                // a chunk of one sub-tile keeps its tile resident across head groups
+                if (nsub > 1) load_subtile(st);
+            }
             const uint32_t ph = uint32_t(loads - 1) & 1u;
             bool got = mbar_wait(kbar, ph, wc, FA_SITE_DECODE_KV);
             if (!__syncthreads_and(got)) {
                 ok = false;
                 break;
             }
-            // ---- scores s = scale * log2(e) * q . k, one warp per key
-            for (int i = warp; i < nk; i += 4) {
-                const T* krow = Ks + i * D + lane * C::EPL;
-                float kf[C::EPL];
-                if constexpr (C::EPL == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(krow);
-                    const float2 f0 = unpack2<T>(w.x), f1 = unpack2<T>(w.y);
-                    kf[0] = f0.x; kf[1] = f0.y; kf[2] = f1.x; kf[3] = f1.y;
-                } else {
-                    const float2 f0 = unpack2<T>(*reinterpret_cast<const uint32_t*>(krow));
-                    kf[0] = f0.x; kf[1] = f0.y;
-                }
+            // ---- scores: thread <-> key, full dot product from the swizzled K tile
+            {
+                const int i = tid;
+                float s[C::GMAX];
 #pragma unroll
-                for (int gi = 0; gi < C::GMAX; ++gi) {
-                    if (gi < G) {
-                        float part = 0.f;
+                for (int gi = 0; gi < C::GMAX; ++gi) s[gi] = 0.f;
 #pragma unroll
-                        for (int e = 0; e < C::EPL; ++e) part = fmaf(qf[gi][e], kf[e], part);
+                for (int half = 0; half < C::NSUB; ++half) {
 #pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            part += __shfl_xor_sync(0xffffffffu, part, off);
-                        if (lane == 0) sc[gi * C::TK + i] = part * a.scale_log2;
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(
+                            Ks + half * C::SUB_BYTES + i * 128 + ((ch ^ (i & 7)) << 4));
+                        float kf[8];
+                        unpack8<T>(w, kf);
+                        const int col = half * 64 + ch * 8;
+#pragma unroll
+                        for (int gi = 0; gi < C::GMAX; ++gi) {
+                            if (gi < G) {
+                                const float4 q0 = *reinterpret_cast<const float4*>(qs + gi * D + col);
+                                const float4 q1 =
+                                    *reinterpret_cast<const float4*>(qs + gi * D + col + 4);
+                                float t = s[gi];
+                                t = fmaf(q0.x, kf[0], t);
+                                t = fmaf(q0.y, kf[1], t);
+                                t = fmaf(q0.z, kf[2], t);
+                                t = fmaf(q0.w, kf[3], t);
+                                t = fmaf(q1.x, kf[4], t);
+                                t = fmaf(q1.y, kf[5], t);
+                                t = fmaf(q1.z, kf[6], t);
+                                t = fmaf(q1.w, kf[7], t);
+                                s[gi] = t;
+                            }
+                        }
                     }
                 }
+#pragma unroll
+                for (int gi = 0; gi < C::GMAX; ++gi)
+                    if (gi < G) sc[gi * C::TK + i] = i < nk ? s[gi] * a.scale_log2 : -INFINITY;
             }
             __syncthreads();
             // ---- softmax update of each head (one warp per head)
@@ -182,8 +210,7 @@ __global__ void __launch_bounds__(128)
                 float mx = -INFINITY;
 #pragma unroll
                 for (int t = 0; t < C::TK / 32; ++t) {
-                    const int i = lane + 32 * t;
-                    v[t] = i < nk ? srow[i] : -INFINITY;
+                    v[t] = srow[lane + 32 * t];
                     mx = fmaxf(mx, v[t]);
                 }
 #pragma unroll
@@ -195,14 +222,12 @@ __global__ void __launch_bounds__(128)
                 float sum = 0.f;
 #pragma unroll
                 for (int t = 0; t < C::TK / 32; ++t) {
-                    const int i = lane + 32 * t;
-                    const float p = i < nk ? fast_exp2(v[t] - m_new) : 0.f;
-                    srow[i] = p;
+                    const float p = fast_exp2(v[t] - m_new);  // masked keys give exp2(-inf) = 0
+                    srow[lane + 32 * t] = p;
                     sum += p;
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                __syncwarp();
                 if (lane == 0) {
                     hm[gi] = m_new;
                     hl[gi] = hl[gi] * alpha + sum;
@@ -214,45 +239,55 @@ __global__ void __launch_bounds__(128)
                 ok = false;
                 break;
             }
-            // ---- O_acc = alpha * O_acc + P V
-#pragma unroll
-            for (int gi = 0; gi < C::GMAX; ++gi)
-                if (gi < G) acc[gi] *= halpha[gi];
-            for (int i = kg; i < nk; i += C::KG) {
-                const float vf = static_cast<float>(Vs[i * D + col]);
-#pragma unroll
-                for (int gi = 0; gi < C::GMAX; ++gi)
-                    if (gi < G) acc[gi] = fmaf(sc[gi * C::TK + i], vf, acc[gi]);
-            }
-            __syncthreads();  // the tile and scores may be overwritten next
-        }
-        if (!ok) break;
-        // ---- combine key groups and write the chunk partials (fp32, log2-domain lse)
-        if constexpr (C::KG > 1) {
-#pragma unroll
-            for (int gi = 0; gi < C::GMAX; ++gi)
-                if (gi < G) red[(gi * C::KG + kg) * D + col] = acc[gi];
-            __syncthreads();
-            if (kg == 0) {
-#pragma unroll
-                for (int gi = 0; gi < C::GMAX; ++gi) {
-                    if (gi < G) {
-                        float t = 0.f;
-#pragma unroll
-                        for (int u = 0; u < C::KG; ++u) t += red[(gi * C::KG + u) * D + col];
-                        acc[gi] = t;
-                    }
-                }
-            }
-        }
-        if (kg == 0) {
+            // ---- O_acc = alpha * O_acc + P V over this thread's key group and column pair
 #pragma unroll
             for (int gi = 0; gi < C::GMAX; ++gi) {
                 if (gi < G) {
+                    const float al = halpha[gi];
+                    acc[gi].x *= al;
+                    acc[gi].y *= al;
+                }
+            }
+            const int j0 = kq * KPG;
+            const int j1 = min(j0 + KPG, nk);
+#pragma unroll 4
+            for (int j = j0; j < j1; ++j) {
+                const float2 vf = unpack2<T>(Vw[j * NCP + cp]);
+#pragma unroll
+                for (int gi = 0; gi < C::GMAX; ++gi) {
+                    if (gi < G) {
+                        const float p = sc[gi * C::TK + j];
+                        acc[gi].x = fmaf(p, vf.x, acc[gi].x);
+                        acc[gi].y = fmaf(p, vf.y, acc[gi].y);
+                    }
+                }
+            }
+            __syncthreads();  // the tile and the scores may be overwritten next
+        }
+        if (!ok) break;
+        // ---- combine the key groups and write the chunk partials (fp32, log2-domain lse)
+        if (kq > 0) {
+#pragma unroll
+            for (int gi = 0; gi < C::GMAX; ++gi)
+                if (gi < G) red[((kq - 1) * C::GMAX + gi) * NCP + cp] = acc[gi];
+        }
+        __syncthreads();
+        if (kq == 0) {
+#pragma unroll
+            for (int gi = 0; gi < C::GMAX; ++gi) {
+                if (gi < G) {
+                    float2 t = acc[gi];
+#pragma unroll
+                    for (int u = 1; u < C::KQ; ++u) {
+                        const float2 o = red[((u - 1) * C::GMAX + gi) * NCP + cp];
+                        t.x += o.x;
+                        t.y += o.y;
+                    }
                     const int h = kvh * g + hg + gi;
                     const size_t pr = (size_t(b) * a.Hq + h) * a.nc + c;
-                    a.o_part[pr * D + col] = acc[gi] / hl[gi];
-                    if (col == 0) a.lse_part[pr] = hm[gi] + log2f(hl[gi]);
+                    const float inv = 1.f / hl[gi];
+                    reinterpret_cast<float2*>(a.o_part + pr * D)[cp] = make_float2(t.x * inv, t.y * inv);
+                    if (cp == 0) a.lse_part[pr] = hm[gi] + log2f(hl[gi]);
                 }
             }
         }
@@ -379,6 +414,28 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns)
 }
 
 }  // namespace
+
+bool encode_decode_maps(EncodeTiledFn enc, const void* k, const void* v, int dtype, int d,
+                        int Hkv, int M, int B, CUtensorMap* tk, CUtensorMap* tv) {
+    // dims innermost first {d, heads, keys, batch}; K in 64-element (128-byte)
+    // swizzled boxes so that thread i reads key row i without bank conflicts,
+    // V as whole unswizzled rows (read row by row).
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)M, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2,
+                                   (cuuint64_t)M * Hkv * d * 2};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType ty =
+        dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint32_t kbox[4] = {64, 1, (cuuint32_t)kDecodeSubTile, 1};
+    const cuuint32_t vbox[4] = {(cuuint32_t)d, 1, (cuuint32_t)kDecodeSubTile, 1};
+    if (enc(tk, ty, 4, const_cast<void*>(k), dims, strides, kbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    return enc(tv, ty, 4, const_cast<void*>(v), dims, strides, vbox, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int d,
                           int dtype, cudaStream_t stream) {

@@ -42,10 +42,7 @@ constexpr size_t kScratchFloats = FA_DECODE_NOALLOC_SCRATCH_BYTES / sizeof(float
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 static __device__ int g_noalloc_status;
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using fa::EncodeTiledFn;
 
 struct DeviceSetup {
     bool done = false;
@@ -108,22 +105,6 @@ fa_status setup_current_device(DeviceSetup** out) {
     return FA_OK;
 }
 
-fa_status encode_kv_map(CUtensorMap* map, const void* base, int dtype, int d, int heads, int seq,
-                        int batch) {
-    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)seq,
-                                (cuuint64_t)batch};
-    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2,
-                                   (cuuint64_t)seq * heads * d * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)d, 1, (cuuint32_t)fa::kDecodeSubTile, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult r = g_encode(
-        map, dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-        4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
-}
-
 }  // namespace
 
 FA_EXPORT fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, void* o,
@@ -151,8 +132,7 @@ FA_EXPORT fa_status fa_decode_noalloc(const void* q, const void* k, const void* 
     fa_status st = setup_current_device(&s);
     if (st != FA_OK) return st;
     CUtensorMap tk, tv;
-    if ((st = encode_kv_map(&tk, k, dtype, d, Hkv, M, B)) != FA_OK) return st;
-    if ((st = encode_kv_map(&tv, v, dtype, d, Hkv, M, B)) != FA_OK) return st;
+    if (!fa::encode_decode_maps(g_encode, k, v, dtype, d, Hkv, M, B, &tk, &tv)) return FA_ERR_CUDA;
     fa::DecodeArgs a{};
     a.q = q;
     a.o = o;

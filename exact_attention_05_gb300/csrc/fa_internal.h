@@ -47,6 +47,16 @@ struct DecodeArgs {
     unsigned long long timeout_ns;
 };
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Encodes the K and V tensor maps the decode chunk kernel reads (their boxes
+// and swizzle are the kernel's business).  Returns false if encoding failed.
+bool encode_decode_maps(EncodeTiledFn enc, const void* k, const void* v, int dtype, int d,
+                        int Hkv, int M, int B, CUtensorMap* tk, CUtensorMap* tv);
+
 // dtype: 0 = fp16, 1 = bf16; d in {64, 128}.
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const PrefillArgs& a, int d, int dtype,
