@@ -100,11 +100,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest() -> str:
+KERNEL_SOURCES = {
+    "prefill_kernel": ["fa_prefill.cu", "fa_device.cuh", "fa_internal.h"],
+    "decode_chunk_kernel": ["fa_decode.cu", "fa_device.cuh", "fa_internal.h"],
+    "decode_merge_kernel": ["fa_decode.cu", "fa_device.cuh", "fa_internal.h"],
+}
+
+
+def kernel_source_digest(kernel: str) -> str:
+    """Short hash of the source files a kernel is compiled from."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_05_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -119,7 +127,7 @@ def recorded_traffic(workload: str, kernel: str):
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(kernel)
     for line in lines:
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload \
@@ -247,6 +255,30 @@ def bench_decode(torch, fa, w, steps, warmup, flush, dist=None):
     if fa.fa_get_last_device_status() != fa.FA_OK:
         raise RuntimeError(f"{w.name}: a device-side wait expired")
     return times
+
+
+def bench_e2e_decode(torch, fa, w, steps, warmup):
+    """Public API with pinned host buffers: H2D of q/k/v, fa_decode, D2H of o/lse."""
+    from exact_attention_05_gb300.workloads import workload_inputs
+    qh, kh, vh = (t.pin_memory() for t in workload_inputs(w))
+    qd, kd, vd = (torch.empty_like(t, device="cuda") for t in (qh, kh, vh))
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    oh = torch.empty_like(qh).pin_memory()
+    lseh = torch.empty((w.B, w.Hq), dtype=torch.float32).pin_memory()
+
+    def call():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        fa.fa_decode(qd, kd, vd, od, lsed, w.B, w.Hq, w.Hkv, w.M, w.d, w.chunk, w.scale, w.dtype)
+        oh.copy_(od, non_blocking=True)
+        lseh.copy_(lsed, non_blocking=True)
+
+    times = time_calls(torch, call, steps, warmup)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lseh.numel() * lseh.element_size()
+    return times, h2d, d2h
 
 
 def bench_e2e_prefill(torch, fa, w, steps, warmup):
@@ -410,17 +442,25 @@ def main(argv=None):
         flush_ctr[0] = (flush_ctr[0] + 1) & 0xFF
         flush_buf.fill_(flush_ctr[0])
 
+    is_decode = w.kind == "decode"
+    # work units of one step: FLOPs (prefill) or HBM bytes (decode), and their scale
+    units, per = (w.decode_bytes, 1e9) if is_decode else (w.flops, 1e12)
     extras = {}
     with ClockSampler(torch.cuda.current_device()) as clocks:
-        times = bench_prefill(torch, fa, w, args.steps, args.warmup, flush, dist)
+        if is_decode:
+            times = bench_decode(torch, fa, w, args.steps, args.warmup,
+                                 flush if units < 4 * FLUSH_BYTES else None, dist)
+        else:
+            times = bench_prefill(torch, fa, w, args.steps, args.warmup, flush, dist)
         mean_ms = sum(times) / len(times)
         mean_ms_max = max_over_ranks(mean_ms, dist, device="cuda")
-        value = aggregate_throughput(w.flops, world, mean_ms_max * 1e-3) / 1e12
+        value = aggregate_throughput(units, world, mean_ms_max * 1e-3) / per
 
         e2e_steps = max(3, min(args.steps, 20))
-        e2e_times, h2d, d2h = bench_e2e_prefill(torch, fa, w, e2e_steps, 3)
+        e2e_fn = bench_e2e_decode if is_decode else bench_e2e_prefill
+        e2e_times, h2d, d2h = e2e_fn(torch, fa, w, e2e_steps, 3)
         e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), dist, device="cuda")
-        e2e_value = aggregate_throughput(w.flops, world, e2e_ms * 1e-3) / 1e12
+        e2e_value = aggregate_throughput(units, world, e2e_ms * 1e-3) / per
 
         if not args.no_extras:
             wd = WORKLOADS[DECODE]
@@ -453,19 +493,37 @@ def main(argv=None):
             extras["workloads"] = table
     clk = clocks.summary()
 
-    if rank == 0 and world == 1 and not args.no_extras:
+    if rank == 0 and world == 1 and not args.no_extras and not is_decode:
         try:
             extras["cpu_baseline"] = cpu_baseline(w)
         except Exception as exc:  # the CPU leg never decides the GPU numbers
             extras["cpu_baseline"] = {"value": None, "unit": "TFLOP/s", "cores": None,
                                       "kind": "oracle", "sample": f"failed: {exc}"}
 
-    achieved = w.flops / (mean_ms_max * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
+    from exact_attention_05_gb300.workloads import DTYPE_NAME
+    achieved = units / (mean_ms_max * 1e-3) / per
+    if is_decode:
+        unit = "GB/s"
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": unit,
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": recorded_traffic(w.name, "decode_chunk_kernel"),
+                "peak_source": f"{peak_src} HBM copy",
+                "note": "achieved over the whole call (chunk + merge kernels)"}
+        l2 = "inputs larger than L2" if units >= 4 * FLUSH_BYTES else \
+            "flushed between steps (256 MiB write)"
+        launches = 2 * args.steps
+    else:
+        unit = "TFLOP/s"
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": unit, "frac": achieved / peaks["bf16_tflops"],
+                "traffic": recorded_traffic(w.name, "prefill_kernel"),
+                "peak_source": f"{peak_src} dense bf16 burst"}
+        l2 = "flushed between steps (256 MiB write)"
+        launches = args.steps
     line = {
         "metric": METRIC,
         "value": value,
-        "unit": "TFLOP/s",
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -473,17 +531,13 @@ def main(argv=None):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": DTYPE_NAME[w.dtype],
         "data": "synthetic",
-        "config": dict(workload_config(w), l2="flushed between steps (256 MiB write)",
-                       parallelism=f"replicas x{world}"),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak,
-                     "traffic": recorded_traffic(w.name, "prefill_kernel"),
-                     "peak_source": f"{peak_src} dense bf16 burst"},
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "config": dict(workload_config(w), l2=l2, parallelism=f"replicas x{world}"),
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": launches,
         "clocks": clk,
     }
     line.update(extras)

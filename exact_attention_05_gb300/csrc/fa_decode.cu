@@ -64,7 +64,7 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
     f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
-template <int D, typename T>
+template <int D, typename T, int GP>
 __global__ void __launch_bounds__(128, 3)
     decode_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
@@ -129,10 +129,12 @@ __global__ void __launch_bounds__(128, 3)
     const int cp = tid % NCP;
     const int kq = tid / NCP;
     constexpr int KPG = C::TK / C::KQ;  // keys per group
-    for (int hg = 0; hg < g && ok; hg += C::GMAX) {
-        const int G = min(C::GMAX, g - hg);
+    // GP query heads per pass; the host picks GP dividing the group size, so
+    // every pass is full and no per-head predicate is needed
+    for (int hg = 0; hg < g && ok; hg += GP) {
+        constexpr int G = GP;
         // this pass's query heads, as fp32 in shared memory (read as broadcasts)
-        for (int e = tid; e < C::GMAX * D; e += C::THREADS) {
+        for (int e = tid; e < GP * D; e += C::THREADS) {
             const int gi = e / D, col = e % D;
             float val = 0.f;
             if (gi < G) {
@@ -146,9 +148,9 @@ __global__ void __launch_bounds__(128, 3)
             hm[tid] = -INFINITY;
             hl[tid] = 0.f;
         }
-        float2 acc[C::GMAX];
+        float2 acc[GP];
 #pragma unroll
-        for (int gi = 0; gi < C::GMAX; ++gi) acc[gi] = make_float2(0.f, 0.f);
+        for (int gi = 0; gi < GP; ++gi) acc[gi] = make_float2(0.f, 0.f);
 
         for (int st = 0; st < nsub; ++st) {
             const int ks = key0 + st * C::TK;
@@ -166,9 +168,9 @@ __global__ void __launch_bounds__(128, 3)
             // ---- scores: thread <-> key, full dot product from the swizzled K tile
             {
                 const int i = tid;
-                float s[C::GMAX];
+                float s[GP];
 #pragma unroll
-                for (int gi = 0; gi < C::GMAX; ++gi) s[gi] = 0.f;
+                for (int gi = 0; gi < GP; ++gi) s[gi] = 0.f;
 #pragma unroll
                 for (int half = 0; half < C::NSUB; ++half) {
 #pragma unroll
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(128, 3)
                         unpack8<T>(w, kf);
                         const int col = half * 64 + ch * 8;
 #pragma unroll
-                        for (int gi = 0; gi < C::GMAX; ++gi) {
+                        for (int gi = 0; gi < GP; ++gi) {
                             if (gi < G) {
                                 const float4 q0 = *reinterpret_cast<const float4*>(qs + gi * D + col);
                                 const float4 q1 =
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(128, 3)
                     }
                 }
 #pragma unroll
-                for (int gi = 0; gi < C::GMAX; ++gi)
+                for (int gi = 0; gi < GP; ++gi)
                     if (gi < G) sc[gi * C::TK + i] = i < nk ? s[gi] * a.scale_log2 : -INFINITY;
             }
             __syncthreads();
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(128, 3)
             }
             // ---- O_acc = alpha * O_acc + P V over this thread's key group and column pair
 #pragma unroll
-            for (int gi = 0; gi < C::GMAX; ++gi) {
+            for (int gi = 0; gi < GP; ++gi) {
                 if (gi < G) {
                     const float al = halpha[gi];
                     acc[gi].x *= al;
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(128, 3)
             for (int j = j0; j < j1; ++j) {
                 const float2 vf = unpack2<T>(Vw[j * NCP + cp]);
 #pragma unroll
-                for (int gi = 0; gi < C::GMAX; ++gi) {
+                for (int gi = 0; gi < GP; ++gi) {
                     if (gi < G) {
                         const float p = sc[gi * C::TK + j];
                         acc[gi].x = fmaf(p, vf.x, acc[gi].x);
@@ -268,13 +270,13 @@ __global__ void __launch_bounds__(128, 3)
         // ---- combine the key groups and write the chunk partials (fp32, log2-domain lse)
         if (kq > 0) {
 #pragma unroll
-            for (int gi = 0; gi < C::GMAX; ++gi)
+            for (int gi = 0; gi < GP; ++gi)
                 if (gi < G) red[((kq - 1) * C::GMAX + gi) * NCP + cp] = acc[gi];
         }
         __syncthreads();
         if (kq == 0) {
 #pragma unroll
-            for (int gi = 0; gi < C::GMAX; ++gi) {
+            for (int gi = 0; gi < GP; ++gi) {
                 if (gi < G) {
                     float2 t = acc[gi];
 #pragma unroll
@@ -298,6 +300,8 @@ __global__ void __launch_bounds__(128, 3)
         mbar_drain_wait(kbar, uint32_t(loads - 1) & 1u, wc, FA_SITE_DRAIN);
         mbar_drain_wait(vbar, uint32_t(loads - 1) & 1u, wc, FA_SITE_DRAIN);
     }
+    // this CTA's partials are written: the merge grid may be scheduled
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Block-wide max and sum over 256 threads (8 warps).
@@ -325,75 +329,107 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
     return r;
 }
 
+// One CTA of 128 threads per (b, h) and 16 output columns: thread t owns the
+// float4 column group t % 4 and the chunks c = t / 4 (mod 32).
 template <int D, typename T>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a) {
-    __shared__ float red[8];
-    __shared__ float4 part[8][32];
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+    // the chunk kernel's partials must be complete and visible (programmatic
+    // dependent launch: this grid may start before the previous one ends)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float red[4];
+    __shared__ float4 part[4][4];
     const int bh = blockIdx.x;
-    const int col0 = blockIdx.y * 32;
+    const int col0 = blockIdx.y * 16;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float* lse_row = a.lse_part + size_t(bh) * a.nc;
     const float* o_rows = a.o_part + size_t(bh) * a.nc * D;
 
     float mx = -INFINITY;
-    for (int cc = tid; cc < a.nc; cc += 256) mx = fmaxf(mx, lse_row[cc]);
-    mx = block_max_256(mx, red);
+    for (int cc = tid; cc < a.nc; cc += 128) mx = fmaxf(mx, lse_row[cc]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
     float sm = 0.f;
-    for (int cc = tid; cc < a.nc; cc += 256) sm += fast_exp2(lse_row[cc] - mx);
-    sm = block_sum_256(sm, red);
+    for (int cc = tid; cc < a.nc; cc += 128) sm += fast_exp2(lse_row[cc] - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
+    if (lane == 0) red[warp] = sm;
+    __syncthreads();
+    sm = red[0] + red[1] + red[2] + red[3];
     const float glse = mx + log2f(sm);  // log2 domain
 
-    // lane -> (4 columns, one of 4 chunks); warp -> chunk offset; 32 chunks per step
-    const int cq = lane & 7;
-    const int csub = lane >> 3;
+    const int cq = tid & 3;
+    const float* src = o_rows + col0 + cq * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int cc = warp * 4 + csub; cc < a.nc; cc += 32) {
+#pragma unroll 8
+    for (int cc = tid >> 2; cc < a.nc; cc += 32) {
         const float w = fast_exp2(lse_row[cc] - glse);
-        const float4 v = *reinterpret_cast<const float4*>(o_rows + size_t(cc) * D + col0 + cq * 4);
+        const float4 v = *reinterpret_cast<const float4*>(src + size_t(cc) * D);
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
         acc.w = fmaf(w, v.w, acc.w);
     }
 #pragma unroll
-    for (int off = 8; off < 32; off <<= 1) {
+    for (int off = 4; off < 32; off <<= 1) {
         acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
         acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
         acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
         acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
     }
-    if (csub == 0) part[warp][cq] = acc;
+    if (lane < 4) part[warp][lane] = acc;
     __syncthreads();
-    if (tid < 8) {
+    if (tid < 4) {
         float4 t = part[0][tid];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) {
+        for (int w = 1; w < 4; ++w) {
             t.x += part[w][tid].x;
             t.y += part[w][tid].y;
             t.z += part[w][tid].z;
             t.w += part[w][tid].w;
         }
         T* orow = reinterpret_cast<T*>(a.o) + size_t(bh) * D + col0 + tid * 4;
-        const uint2 packed = make_uint2(pack2<T>(t.x, t.y), pack2<T>(t.z, t.w));
-        *reinterpret_cast<uint2*>(orow) = packed;
+        *reinterpret_cast<uint2*>(orow) = make_uint2(pack2<T>(t.x, t.y), pack2<T>(t.z, t.w));
     }
     if (tid == 0 && blockIdx.y == 0 && a.lse != nullptr) a.lse[bh] = glse * kLn2;
+}
+
+template <int D, typename T, int GP>
+cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                         cudaStream_t stream) {
+    using C = DecodeCfg<D>;
+    auto kern = decode_chunk_kernel<D, T, GP>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    kern<<<dim3(a.nc, a.B * a.Hkv), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tk, tv, a);
+    return cudaGetLastError();
 }
 
 template <int D, typename T>
 cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                             cudaStream_t stream) {
-    using C = DecodeCfg<D>;
-    auto chunk_kern = decode_chunk_kernel<D, T>;
-    cudaError_t err = cudaFuncSetAttribute(chunk_kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::SMEM_BYTES);
+    const int g = a.Hq / a.Hkv;
+    cudaError_t err = (g % 4 == 0)   ? launch_chunk<D, T, 4>(tk, tv, a, stream)
+                      : (g % 2 == 0) ? launch_chunk<D, T, 2>(tk, tv, a, stream)
+                                     : launch_chunk<D, T, 1>(tk, tv, a, stream);
     if (err != cudaSuccess) return err;
-    chunk_kern<<<dim3(a.nc, a.B * a.Hkv), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tk, tv, a);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    decode_merge_kernel<D, T><<<dim3(a.B * a.Hq, D / 32), dim3(256), 0, stream>>>(a);
-    return cudaGetLastError();
+    // the merge is launched as a programmatic dependent of the chunk grid so that
+    // its launch overlaps the chunk grid's tail; it waits for the data itself
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.B * a.Hq, D / 16);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, T>, a);
 }
 
 __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns) {
