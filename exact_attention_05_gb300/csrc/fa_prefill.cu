@@ -12,23 +12,28 @@
 // discussion, so that most tiles touch O not at all.
 //
 // How it runs on GB300 (not the page's design, which used ldmatrix + mma.sync):
-//   * one CTA per 128-row Q tile, 6 warps with fixed roles:
-//       warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t);
-//                  it reads its S row from TMEM, masks, updates m/l, writes
-//                  P (fp16/bf16) back into TMEM, rescales its O row when
-//                  needed, and runs the epilogue (O / l -> smem -> TMA store,
-//                  LSE -> global);
-//       warp 4     TMA producer: Q once, then K/V tiles into a ring of
-//                  shared-memory slots in the order the MMA consumes them;
-//       warp 5     TMEM allocator and single-thread tcgen05 MMA issuer.
-//   * S = Q K^T and O += P V run on the 5th-gen tensor core (tcgen05.mma,
-//     M = 128) with fp32 accumulators in TMEM; S is double-buffered so the
-//     MMA of tile j+1 overlaps the softmax of tile j, and P is read by the PV
-//     MMA straight from TMEM (A operand in tensor memory), never from smem.
+//   * one CTA per pair of 128-row Q tiles of one (b, h) -- 256 query rows --
+//     sharing every K/V tile; 10 warps with fixed roles:
+//       warps 0-3  softmax of Q tile 0, warps 4-7 softmax of Q tile 1: thread
+//                  t of a warpgroup owns query row t of its tile (TMEM lane
+//                  t); it reads its S row from TMEM, masks, updates m/l,
+//                  writes P (fp16/bf16) back into TMEM over the upper half
+//                  of its S row, rescales its O row when needed, and runs
+//                  the epilogue (O / l -> smem -> TMA store, LSE -> global);
+//       warp 8     TMA producer: Q0, Q1 once, then K0, V0, K1, V1, ... into a
+//                  ring of shared-memory slots;
+//       warp 9     TMEM allocator and single-thread tcgen05 MMA issuer.
+//   * the tensor core ping-pongs between the tiles:
+//       ... PV0(j)  QK0(j+1)  PV1(j)  QK1(j+1)  PV0(j+1) ...
+//     so the softmax of one tile (S -> P) runs while the other tile's two
+//     GEMMs execute; S = Q K^T and O += P V accumulate in fp32 in TMEM, and P
+//     is read by the PV MMA straight from TMEM (A operand in tensor memory).
+//   * TMEM map (512 columns): S0 [0,128) with P0 in [64,128), S1 [128,256)
+//     with P1 in [192,256), O0 [256,256+d), O1 [256+d,256+2d).  QKi(j+1)
+//     overwrites the P_i that PVi(j) reads; tcgen05.mma operations issued by
+//     one thread execute in issue order, and PVi(j) is issued first.
 //   * K/V/Q tiles are 128-byte-swizzled 64-column halves written by TMA and
 //     read by the MMA through shared-memory descriptors.
-//   * TMEM map (512 columns): S0 [0,128), S1 [128,256), O [256,256+d),
-//     P0 and P1 (64 columns each, two 16-bit values per column) after O.
 //   * every wait is bounded; on expiry the CTA records the timeout, drains
 //     its own copies and MMAs, frees TMEM and returns.
 
@@ -43,38 +48,37 @@ namespace {
 
 template <int D>
 struct PrefillCfg {
-    static constexpr int BM = 128;
-    static constexpr int BN = 128;
+    static constexpr int BM = 128;                         // rows per Q tile
+    static constexpr int BN = 128;                         // keys per KV tile
+    static constexpr int NQ = 2;                           // Q tiles per CTA
     static constexpr int NSUB = D / 64;                    // 64-element (128 B) column halves
     static constexpr int SUB_BYTES = 128 * 128;            // 128 rows x 128 B
     static constexpr int TILE_BYTES = NSUB * SUB_BYTES;    // one Q, K or V tile
     static constexpr int NSLOT = D == 128 ? 5 : 8;         // K/V ring depth
-    static constexpr int Q_OFF = 0;
-    static constexpr int SLOT_OFF = TILE_BYTES;
+    static constexpr int Q_OFF = 0;                        // Q0, Q1
+    static constexpr int SLOT_OFF = NQ * TILE_BYTES;
     static constexpr int BAR_OFF = SLOT_OFF + NSLOT * TILE_BYTES;
     // barrier indices
     static constexpr int B_QFULL = 0;
     static constexpr int B_FULL = 1;                       // NSLOT of them
     static constexpr int B_EMPTY = 1 + NSLOT;              // NSLOT of them
-    static constexpr int B_SFULL = 1 + 2 * NSLOT;          // 2
-    static constexpr int B_PFULL = 3 + 2 * NSLOT;          // 2
-    static constexpr int B_ODONE = 5 + 2 * NSLOT;
-    static constexpr int B_DRAIN = 6 + 2 * NSLOT;
-    static constexpr int NBAR = 7 + 2 * NSLOT;
+    static constexpr int B_SFULL = 1 + 2 * NSLOT;          // one per Q tile
+    static constexpr int B_PFULL = 3 + 2 * NSLOT;          // one per Q tile
+    static constexpr int B_ODONE = 5 + 2 * NSLOT;          // one per Q tile
+    static constexpr int B_DRAIN = 7 + 2 * NSLOT;
+    static constexpr int NBAR = 8 + 2 * NSLOT;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
     // TMEM columns
-    static constexpr uint32_t TM_S0 = 0;
-    static constexpr uint32_t TM_S1 = 128;
-    static constexpr uint32_t TM_O = 256;
-    static constexpr uint32_t TM_P0 = 256 + D;
-    static constexpr uint32_t TM_P1 = 256 + D + 64;
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(TM_P1 + 64 <= TMEM_COLS, "TMEM budget");
+    __host__ __device__ static constexpr uint32_t tm_s(int i) { return 128u * i; }
+    __host__ __device__ static constexpr uint32_t tm_p(int i) { return 128u * i + 64u; }
+    __host__ __device__ static constexpr uint32_t tm_o(int i) { return 256u + D * i; }
+    static_assert(256 + 2 * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
@@ -96,17 +100,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Which tile: the latest (most expensive, when causal) query tiles go first.
+    // Which pair of Q tiles: the latest (most expensive, when causal) pairs go first.
+    const int npairs = (a.n_qtiles + 1) / 2;
     const int nbh = a.B * a.Hq;
     const int lin = blockIdx.x;
-    const int qt = a.n_qtiles - 1 - lin / nbh;
+    const int pt = npairs - 1 - lin / nbh;
     const int bh = lin % nbh;
     const int h = bh % a.Hq;
     const int b = bh / a.Hq;
     const int kvh = h / (a.Hq / a.Hkv);
-    const int q0 = qt * C::BM;
-    const int kv_end = a.causal ? min(a.M, q0 + C::BM) : a.M;
-    const int nt = (kv_end + C::BN - 1) / C::BN;
+    const int q0 = pt * (C::NQ * C::BM);
+    const bool t1 = q0 + C::BM < a.N;  // is Q tile 1 inside the sequence?
+    auto ntiles = [&](int i) -> int {
+        const int kv_end = a.causal ? min(a.M, q0 + (i + 1) * C::BM) : a.M;
+        return (kv_end + C::BN - 1) / C::BN;
+    };
+    const int nt0 = ntiles(0);
+    const int nt = t1 ? ntiles(1) : nt0;  // KV tiles the CTA walks (nt >= nt0)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
@@ -114,22 +124,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::B_FULL + i), 1);
             mbar_init(bar(C::B_EMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NQ; ++i) {
             mbar_init(bar(C::B_SFULL + i), 1);
             mbar_init(bar(C::B_PFULL + i), 128);
+            mbar_init(bar(C::B_ODONE + i), 1);
         }
-        mbar_init(bar(C::B_ODONE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         prefetch_tensor_map(&tm_q);
         prefetch_tensor_map(&tm_k);
         prefetch_tensor_map(&tm_v);
         prefetch_tensor_map(&tm_o);
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_addr(const_cast<uint32_t*>(tmem_holder)), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -139,32 +149,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const WaitCtl wc{abort_flag, a.status, a.timeout_ns};
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------- producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE_BYTES);
-            for (int s = 0; s < C::NSUB; ++s)
-                tma_load_4d(sbase + C::Q_OFF + s * C::SUB_BYTES, &tm_q, s * 64, h, q0, b,
-                            bar(C::B_QFULL));
-            int L = 0;  // loads issued, in consumption order K0, K1, V0, K2, V1, ...
-            auto issue = [&](bool is_v, int j) -> bool {
+            mbar_arrive_expect_tx(bar(C::B_QFULL), (t1 ? 2 : 1) * C::TILE_BYTES);
+            for (int i = 0; i < (t1 ? 2 : 1); ++i)
+                for (int s = 0; s < C::NSUB; ++s)
+                    tma_load_4d(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q,
+                                s * 64, h, q0 + i * C::BM, b, bar(C::B_QFULL));
+            int L = 0;  // loads issued: K0, V0, K1, V1, ...
+            bool ok = true;
+            for (; ok && L < 2 * nt; ++L) {
                 const int slot = L % C::NSLOT;
                 const uint32_t parity = ((L / C::NSLOT) & 1) ^ 1;
-                if (!mbar_wait(bar(C::B_EMPTY + slot), parity, wc, FA_SITE_PRODUCER_SLOT))
-                    return false;
+                if (!mbar_wait(bar(C::B_EMPTY + slot), parity, wc, FA_SITE_PRODUCER_SLOT)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE_BYTES);
                 const uint32_t dst = sbase + C::SLOT_OFF + slot * C::TILE_BYTES;
+                const CUtensorMap* map = (L & 1) ? &tm_v : &tm_k;
                 for (int s = 0; s < C::NSUB; ++s)
-                    tma_load_4d(dst + s * C::SUB_BYTES, is_v ? &tm_v : &tm_k, s * 64, kvh, j * C::BN,
-                                b, bar(C::B_FULL + slot));
-                ++L;
-                return true;
-            };
-            bool ok = issue(false, 0);
-            if (ok && nt > 1) ok = issue(false, 1);
-            for (int j = 0; ok && j < nt; ++j) {
-                ok = issue(true, j);
-                if (ok && j + 2 < nt) ok = issue(false, j + 2);
+                    tma_load_4d(dst + s * C::SUB_BYTES, map, s * 64, kvh, (L >> 1) * C::BN, b,
+                                bar(C::B_FULL + slot));
             }
             // Every issued copy must have landed before the CTA may exit.
             mbar_drain_wait(bar(C::B_QFULL), 0, wc, FA_SITE_DRAIN);
@@ -173,66 +180,100 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_drain_wait(bar(C::B_FULL + slot), (last / C::NSLOT) & 1, wc, FA_SITE_DRAIN);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t fmt = DTypeFmt<T>::value;
             constexpr uint32_t idesc_qk = instr_desc_f16(fmt, 128, 128, 0, 0);  // Q, K both K-major
             constexpr uint32_t idesc_pv = instr_desc_f16(fmt, 128, D, 0, 1);    // V is MN-major
-            const uint32_t qb = sbase + C::Q_OFF;
-            int L = 0;
-            auto qk = [&](int j) -> bool {
-                const int slot = L % C::NSLOT;
-                if (!mbar_wait(bar(C::B_FULL + slot), (L / C::NSLOT) & 1, wc, FA_SITE_MMA_KV))
-                    return false;
-                tc_fence_after();
-                const uint32_t kb = sbase + C::SLOT_OFF + slot * C::TILE_BYTES;
-                const uint32_t d_tmem = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0);
+            auto slot_of = [](int L) { return L % C::NSLOT; };
+            auto phase_of = [](int L) { return uint32_t(L / C::NSLOT) & 1u; };
+            auto slot_addr = [&](int L) { return sbase + C::SLOT_OFF + slot_of(L) * C::TILE_BYTES; };
+            // S_i = Q_i K^T from the K tile of load L
+            auto qk = [&](int i, int L) {
+                const uint32_t qb = sbase + C::Q_OFF + i * C::TILE_BYTES;
+                const uint32_t kb = slot_addr(L);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // K-major, 128-byte swizzle: k-steps of 16 elements advance 32 bytes
                     // inside a 64-column half; 8-row groups are 1024 bytes apart.
                     const uint32_t off = (kk / 4) * C::SUB_BYTES + (kk % 4) * 32;
-                    mma_ss(d_tmem, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
-                           idesc_qk, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::tm_s(i), smem_desc(qb + off, 16, 1024),
+                           smem_desc(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(C::B_EMPTY + slot));
-                mma_commit(bar(C::B_SFULL + (j & 1)));
-                ++L;
-                return true;
+                mma_commit(bar(C::B_SFULL + i));
             };
-            bool ok = mbar_wait(bar(C::B_QFULL), 0, wc, FA_SITE_MMA_Q);
-            if (ok) tc_fence_after();
-            if (ok) ok = qk(0);
-            if (ok && nt > 1) ok = qk(1);
-            for (int j = 0; ok && j < nt; ++j) {
-                if (!mbar_wait(bar(C::B_PFULL + (j & 1)), (j >> 1) & 1, wc, FA_SITE_MMA_P)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const int slot = L % C::NSLOT;
-                if (!mbar_wait(bar(C::B_FULL + slot), (L / C::NSLOT) & 1, wc, FA_SITE_MMA_KV)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t vb = sbase + C::SLOT_OFF + slot * C::TILE_BYTES;
-                const uint32_t p_tmem = tmem + ((j & 1) ? C::TM_P1 : C::TM_P0);
+            // O_i (+)= P_i V from the V tile of load L
+            auto pv = [&](int i, int L, bool accumulate) {
+                const uint32_t vb = slot_addr(L);
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
                     // V is [key][d] = MN-major for B (N = d): 16 keys = 16 rows of 128 B;
                     // the two 64-column halves are SUB_BYTES apart (leading offset),
                     // 8-key groups 1024 bytes apart (stride offset).  P: 16 keys of
                     // 16-bit values = 8 TMEM columns.
-                    mma_ts(tmem + C::TM_O, p_tmem + kk * 8,
+                    mma_ts(tmem + C::tm_o(i), tmem + C::tm_p(i) + kk * 8,
                            smem_desc(vb + kk * 16 * 128, C::SUB_BYTES, 1024), idesc_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                           (accumulate || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(C::B_EMPTY + slot));
-                mma_commit(bar(C::B_ODONE));
-                ++L;
-                if (j + 2 < nt) ok = qk(j + 2);
+                mma_commit(bar(C::B_ODONE + i));
+            };
+            auto wait_full = [&](int L) -> bool {
+                if (!mbar_wait(bar(C::B_FULL + slot_of(L)), phase_of(L), wc, FA_SITE_MMA_KV))
+                    return false;
+                tc_fence_after();
+                return true;
+            };
+            auto release = [&](int L) { mma_commit(bar(C::B_EMPTY + slot_of(L))); };
+
+            bool ok = mbar_wait(bar(C::B_QFULL), 0, wc, FA_SITE_MMA_Q);
+            if (ok) tc_fence_after();
+            if (ok) ok = wait_full(0);
+            if (ok) {
+                qk(0, 0);
+                if (t1) qk(1, 0);
+                release(0);  // K0
+            }
+            for (int j = 0; ok && j < nt; ++j) {
+                const int LV = 2 * j + 1, LK = 2 * j + 2;
+                bool have_v = false, have_k = false;
+                if (j < nt0) {
+                    if (!mbar_wait(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P) || !wait_full(LV)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    have_v = true;
+                    pv(0, LV, j > 0);
+                    if (!t1) release(LV);
+                    if (j + 1 < nt0) {
+                        if (!wait_full(LK)) {
+                            ok = false;
+                            break;
+                        }
+                        have_k = true;
+                        qk(0, LK);
+                        if (!t1) release(LK);
+                    }
+                }
+                if (t1) {
+                    if (!mbar_wait(bar(C::B_PFULL + 1), j & 1, wc, FA_SITE_MMA_P) ||
+                        (!have_v && !wait_full(LV))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    pv(1, LV, j > 0);
+                    release(LV);
+                    if (j + 1 < nt) {
+                        if (!have_k && !wait_full(LK)) {
+                            ok = false;
+                            break;
+                        }
+                        qk(1, LK);
+                        release(LK);
+                    }
+                }
             }
             // All MMAs must be complete before TMEM is released.
             mma_commit(bar(C::B_DRAIN));
@@ -240,15 +281,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------- softmax
-        const int r = threadIdx.x;  // row in tile == TMEM lane
-        const int row = q0 + r;
-        const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+        const int tile = warp >> 2;  // 0 or 1
+        const int r = threadIdx.x & 127;  // row in tile == TMEM lane
+        const int row0 = q0 + tile * C::BM;
+        const int row = row0 + r;
+        const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
+        const int nti = tile == 0 ? nt0 : nt;
+        const bool active = tile == 0 || t1;
         const float sl2 = a.scale_log2;
         float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled logits
         float l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nt; ++j) {
-            bool got = mbar_wait(bar(C::B_SFULL + (j & 1)), (j >> 1) & 1, wc, FA_SITE_SOFTMAX_S);
+        bool ok = active;
+        for (int j = 0; ok && j < nti; ++j) {
+            bool got = mbar_wait(bar(C::B_SFULL + tile), j & 1, wc, FA_SITE_SOFTMAX_S);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
@@ -256,28 +301,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             float s[C::BN];
             {
-                const uint32_t s_addr = lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
+                const uint32_t s_addr = lane_base + C::tm_s(tile);
 #pragma unroll
                 for (int c = 0; c < C::BN / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(s_addr + c * 32, v);
-                    tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
                 }
+                tmem_wait_ld();
             }
             const int k0 = j * C::BN;
-            if (k0 + C::BN > a.M || (a.causal && k0 + C::BN - 1 > q0)) {
+            if (k0 + C::BN > a.M || (a.causal && k0 + C::BN - 1 > row0)) {
                 int lim = a.M - k0;
                 if (a.causal) lim = min(lim, row - k0 + 1);
 #pragma unroll
                 for (int c = 0; c < C::BN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            float mx = -INFINITY;
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < C::BN; ++c) mx = fmaxf(mx, s[c]);
-            const float mt = mx * sl2;
+            for (int c = 0; c < C::BN; c += 2) {
+                mx0 = fmaxf(mx0, s[c]);
+                mx1 = fmaxf(mx1, s[c + 1]);
+            }
+            const float mt = fmaxf(mx0, mx1) * sl2;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -289,56 +337,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rescale = true;
             }
             if (__any_sync(0xffffffffu, rescale)) {
-                // O must hold every PV product so far before it is scaled.
-                got = mbar_wait(bar(C::B_ODONE), (j - 1) & 1, wc, FA_SITE_SOFTMAX_O);
+                // O must hold every PV product so far before it is scaled: PV(j-1)
+                // was issued before QK(j), whose completion we just waited for.
+                got = mbar_wait(bar(C::B_ODONE + tile), (j - 1) & 1, wc, FA_SITE_SOFTMAX_O);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t o_addr = lane_base + C::TM_O;
+                const uint32_t o_addr = lane_base + C::tm_o(tile);
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(o_addr + c * 32, v);
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(o_addr + c * 16, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(o_addr + c * 32, v);
+                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st16(o_addr + c * 16, v);
                 }
                 tmem_wait_st();
             }
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint32_t p_addr = lane_base + ((j & 1) ? C::TM_P1 : C::TM_P0);
+            const uint32_t p_addr = lane_base + C::tm_p(tile);
+            float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = fast_exp2(fmaf(s[half * 64 + 2 * e], sl2, neg));
-                    const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * e + 1], sl2, neg));
-                    l += p0 + p1;
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = fast_exp2(fmaf(s[q4 * 32 + 2 * e], sl2, neg));
+                    const float p1 = fast_exp2(fmaf(s[q4 * 32 + 2 * e + 1], sl2, neg));
+                    l0 += p0;
+                    l1 += p1;
                     pk[e] = pack2<T>(p0, p1);
                 }
-                tmem_st32(p_addr + half * 32, pk);
+                tmem_st16(p_addr + q4 * 16, pk);
             }
+            l += l0 + l1;
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL + (j & 1)));
+            mbar_arrive(bar(C::B_PFULL + tile));
         }
         // ------------------------------------------------------------ epilogue
         if (ok) {
-            // The drain barrier completes once, after every MMA of the tile (the
-            // per-PV barrier could alias phases here: the last two PVs may both
-            // still be in flight).
-            const bool got = mbar_wait(bar(C::B_DRAIN), 0, wc, FA_SITE_SOFTMAX_O);
+            // PV(nti-2) completed before QK(nti-1) did, so the barrier is at the
+            // phase of PV(nti-1) now.
+            const bool got =
+                mbar_wait(bar(C::B_ODONE + tile), (nti - 1) & 1, wc, FA_SITE_SOFTMAX_O);
             ok = __all_sync(0xffffffffu, got);
         }
+        uint8_t* stage = smem + C::Q_OFF + tile * C::TILE_BYTES;  // Q_i is dead by now
         if (ok) {
             tc_fence_after();
             const float inv_l = 1.f / l;
-            const uint32_t o_addr = lane_base + C::TM_O;
-            uint8_t* stage = smem + C::Q_OFF;  // Q is dead once the last MMA has completed
+            const uint32_t o_addr = lane_base + C::tm_o(tile);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
@@ -364,10 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 a.lse[(size_t(b) * a.Hq + h) * a.N + row] = (m_ref + log2f(l)) * kLn2;
         }
         fence_async_shared();
-        named_barrier_sync(1, 128);
-        if (threadIdx.x == 0 && *abort_flag == 0) {
+        named_barrier_sync(1 + tile, 128);
+        if (r == 0 && ok && *abort_flag == 0) {
             for (int s = 0; s < C::NSUB; ++s)
-                tma_store_4d(&tm_o, sbase + C::Q_OFF + s * C::SUB_BYTES, s * 64, h, q0, b);
+                tma_store_4d(&tm_o, smem_addr(stage) + s * C::SUB_BYTES, s * 64, h, row0, b);
             tma_store_commit();
             tma_store_wait_all();
         }
@@ -375,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -390,7 +442,7 @@ cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    const long long nblocks = (long long)a.n_qtiles * a.B * a.Hq;
+    const long long nblocks = (long long)((a.n_qtiles + 1) / 2) * a.B * a.Hq;
     if (nblocks <= 0 || nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<dim3((unsigned)nblocks), dim3(kThreads), C::SMEM_BYTES, stream>>>(tq, tk, tv, to, a);
     return cudaGetLastError();
