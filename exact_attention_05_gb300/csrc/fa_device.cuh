@@ -34,6 +34,37 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Two fp32 lanes in one 64-bit register, for the packed .f32x2 arithmetic of sm_100+.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + c on both lanes (round to nearest).
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -110,17 +141,20 @@ struct WaitCtl {
 };
 
 // Records a timeout: first in the global status word, then in the CTA's abort
-// flag so that every other role of the CTA stops waiting too.
-__device__ __forceinline__ void record_timeout(const WaitCtl& w, int where) {
-    atomicCAS(w.status, 0, FA_DEV_TIMEOUT | (where << 8));
-    *w.abort_flag = 1;
+// flag so that every other role of the CTA stops waiting too.  Kept out of
+// line: it only runs when something has already gone wrong.
+static __device__ __noinline__ void record_timeout(volatile int* abort_flag, int* status,
+                                                   int where) {
+    atomicCAS(status, 0, FA_DEV_TIMEOUT | (where << 8));
+    *abort_flag = 1;
 }
 
 // Waits until the phase of `bar` with the given parity has completed.  Returns
 // false (without waiting further) once the CTA is aborting or after
-// w.timeout_ns of wall time, in which case the timeout is recorded.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w,
-                                       int where) {
+// w.timeout_ns of wall time, in which case the timeout is recorded.  Inline,
+// so that a wait inside a register-heavy loop costs no call.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                          int where) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -128,7 +162,7 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, con
         if ((it & 15u) == 0) {
             if (*w.abort_flag) return false;
             if (global_timer_ns() - t0 > w.timeout_ns) {
-                record_timeout(w, where);
+                record_timeout(w.abort_flag, w.status, where);
                 return false;
             }
         }
@@ -137,12 +171,12 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, con
 
 // Same, but ignores the abort flag: used while draining in-flight copies and
 // MMAs before the CTA exits, still bounded by the timeout.
-static __device__ __noinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& w,
-                                             int where) {
+__device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                                int where) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (global_timer_ns() - t0 > w.timeout_ns) {
-            record_timeout(w, where);
+            record_timeout(w.abort_flag, w.status, where);
             return false;
         }
     }

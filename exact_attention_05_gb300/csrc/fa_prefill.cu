@@ -319,13 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::BN; ++c)
                     if (c >= lim) s[c] = -INFINITY;
             }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            // row max: four independent chains of three-input max
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < C::BN; c += 2) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
+            for (int c = 0; c < C::BN; c += 8) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], s[c + 2 * u], s[c + 2 * u + 1]);
             }
-            const float mt = fmaxf(mx0, mx1) * sl2;
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -359,21 +360,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const uint32_t p_addr = lane_base + C::tm_p(tile);
-            float l0 = 0.f, l1 = 0.f;
+            // p = exp2(s * scale * log2(e) - m_ref), two lanes per packed FMA/ADD
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negx2 = f2_pack(neg, neg);
+            uint64_t lsum[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(fmaf(s[q4 * 32 + 2 * e], sl2, neg));
-                    const float p1 = fast_exp2(fmaf(s[q4 * 32 + 2 * e + 1], sl2, neg));
-                    l0 += p0;
-                    l1 += p1;
+                    const int c = q4 * 32 + 2 * e;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negx2), x0, x1);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    lsum[e & 1] = f2_add(lsum[e & 1], f2_pack(p0, p1));
                     pk[e] = pack2<T>(p0, p1);
                 }
                 tmem_st16(p_addr + q4 * 16, pk);
             }
-            l += l0 + l1;
+            {
+                float a0, a1, b0, b1;
+                f2_unpack(lsum[0], a0, a1);
+                f2_unpack(lsum[1], b0, b1);
+                l += (a0 + a1) + (b0 + b1);
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_PFULL + tile));
