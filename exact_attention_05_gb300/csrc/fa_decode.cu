@@ -304,31 +304,6 @@ __global__ void __launch_bounds__(128, 3)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Block-wide max and sum over 256 threads (8 warps).
-__device__ __forceinline__ float block_max_256(float v, float* red) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = red[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
-    __syncthreads();
-    return r;
-}
-
-__device__ __forceinline__ float block_sum_256(float v, float* red) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) r += red[w];
-    __syncthreads();
-    return r;
-}
-
 // One CTA of 128 threads per (b, h) and 16 output columns: thread t owns the
 // float4 column group t % 4 and the chunks c = t / 4 (mod 32).
 template <int D, typename T>
