@@ -88,9 +88,13 @@ __global__ void __launch_bounds__(128, 3)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int c = blockIdx.x;
-    const int b = blockIdx.y / a.Hkv;
-    const int kvh = blockIdx.y % a.Hkv;
+    // Linear block index, (b, kv head) fastest: CTAs that run together read the
+    // neighbouring heads of the same keys, i.e. whole contiguous key rows of the
+    // [B, M, Hkv, d] layout instead of one 2*d-byte slice every Hkv*d*2 bytes.
+    const int nbh = a.B * a.Hkv;
+    const int c = blockIdx.x / nbh;
+    const int b = (blockIdx.x % nbh) / a.Hkv;
+    const int kvh = blockIdx.x % a.Hkv;
     const int g = a.Hq / a.Hkv;
     const int key0 = c * a.chunk;
     const int key1 = min(a.M, key0 + a.chunk);
@@ -380,7 +384,9 @@ cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    kern<<<dim3(a.nc, a.B * a.Hkv), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tk, tv, a);
+    const long long nblocks = (long long)a.nc * a.B * a.Hkv;
+    if (nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<dim3((unsigned)nblocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
