@@ -65,6 +65,8 @@ def load_library():
         lib.fa_fwd.restype = I
         lib.fa_decode.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
         lib.fa_decode.restype = I
+        lib.fa_decode_fused.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
+        lib.fa_decode_fused.restype = I
         lib.fa_decode_noalloc.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
         lib.fa_decode_noalloc.restype = I
         lib.fa_status_string.argtypes = [I]
@@ -126,6 +128,15 @@ def fa_decode(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, stream=Non
     return _check(st, "fa_decode") if check else st
 
 
+def fa_decode_fused(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, stream=None,
+                    check=True) -> int:
+    """fa_decode in one launch: the chunk kernel merges its own partials."""
+    st = load_library().fa_decode_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                        int(Hq), int(Hkv), int(M), int(d), int(chunk),
+                                        float(scale), int(dtype), _stream(stream))
+    return _check(st, "fa_decode_fused") if check else st
+
+
 def fa_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, stream=None,
                       check=True) -> int:
     """fa_decode with its partials in the library's static device scratch: for
@@ -183,8 +194,10 @@ def attention_forward(q, k, v, causal: bool, scale: float, out=None, lse=None, w
     return out, lse
 
 
-def decode(q, k, v, chunk: int, scale: float, out=None, lse=None, with_lse=True, stream=None):
-    """Split-KV decode of q [B,1,Hq,d] against k/v [B,M,Hkv,d]."""
+def decode(q, k, v, chunk: int, scale: float, out=None, lse=None, with_lse=True, stream=None,
+           single_launch=False):
+    """Split-KV decode of q [B,1,Hq,d] against k/v [B,M,Hkv,d] (fa_decode, or
+    fa_decode_fused with ``single_launch``)."""
     import torch
     B, one, Hq, d = q.shape
     if one != 1:
@@ -194,5 +207,6 @@ def decode(q, k, v, chunk: int, scale: float, out=None, lse=None, with_lse=True,
         out = torch.empty_like(q)
     if lse is None and with_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    fa_decode(q, k, v, out, lse, B, Hq, Hkv, M, d, chunk, scale, _dtype_code(q), stream)
+    fn = fa_decode_fused if single_launch else fa_decode
+    fn(q, k, v, out, lse, B, Hq, Hkv, M, d, chunk, scale, _dtype_code(q), stream)
     return out, lse

@@ -26,6 +26,8 @@ std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
+    int* tickets = nullptr;  // zero between calls (the single-launch decode resets what it uses)
+    size_t nticket = 0;
 };
 
 struct DeviceState {
@@ -139,6 +141,31 @@ fa_status workspace(DeviceState* st, cudaStream_t stream, size_t bytes, void** o
     return FA_OK;
 }
 
+// Ticket counters of at least `count` ints for (device, stream), zero on return.
+fa_status tickets(DeviceState* st, cudaStream_t stream, size_t count, int** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace& w = st->workspaces[stream];
+    if (w.nticket < count) {
+        if (w.tickets != nullptr) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+            cudaFree(w.tickets);
+            w.tickets = nullptr;
+            w.nticket = 0;
+        }
+        const size_t want = (count + 4095) & ~size_t(4095);
+        if (cudaMalloc(&w.tickets, want * sizeof(int)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            w.tickets = nullptr;
+            return FA_ERR_NO_MEMORY;
+        }
+        if (cudaMemsetAsync(w.tickets, 0, want * sizeof(int), stream) != cudaSuccess)
+            return FA_ERR_CUDA;
+        w.nticket = want;
+    }
+    *out = w.tickets;
+    return FA_OK;
+}
+
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
@@ -207,6 +234,50 @@ FA_EXPORT fa_status fa_decode(const void* q, const void* k, const void* v, void*
     return from_cuda(fa::launch_decode(tk, tv, a, d, (int)dtype, (cudaStream_t)stream));
 }
 
+FA_EXPORT fa_status fa_decode_fused(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, int B, int Hq, int Hkv, int M, int d, int chunk,
+                                    float scale, fa_dtype dtype, fa_stream_t stream) {
+    fa_status s = check_args(q, k, v, o, lse, B, Hq, Hkv, 1, M, d, scale, (int)dtype);
+    if (s != FA_OK) return s;
+    if (chunk <= 0) return FA_ERR_INVALID_ARG;
+    const long long nc = ((long long)M + chunk - 1) / chunk;
+    if (nc * B * Hkv > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    const int ngroups = (int)((nc + fa::kDecodeMergeGroup - 1) / fa::kDecodeMergeGroup);
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != FA_OK) return s;
+    const size_t part_elems = (size_t)B * Hq * nc * d;
+    const size_t grp_elems = (size_t)B * Hq * ngroups * d;
+    const size_t floats = part_elems + (size_t)B * Hq * nc + grp_elems + (size_t)B * Hq * ngroups;
+    void* ws = nullptr;
+    if ((s = workspace(st, (cudaStream_t)stream, floats * sizeof(float), &ws)) != FA_OK) return s;
+    int* tk_counts = nullptr;
+    if ((s = tickets(st, (cudaStream_t)stream, (size_t)B * Hkv * (ngroups + 1), &tk_counts)) != FA_OK)
+        return s;
+    CUtensorMap tk, tv;
+    if (!fa::encode_decode_maps(g_encode, k, v, dtype, d, Hkv, M, B, &tk, &tv)) return FA_ERR_CUDA;
+    fa::DecodeArgs a{};
+    float* f = static_cast<float*>(ws);
+    a.q = q;
+    a.o = o;
+    a.lse = lse;
+    a.o_part = f;
+    a.lse_part = f + part_elems;
+    a.g_o = a.lse_part + (size_t)B * Hq * nc;
+    a.g_lse = a.g_o + grp_elems;
+    a.tickets = tk_counts;
+    a.ngroups = ngroups;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.M = M;
+    a.chunk = chunk;
+    a.nc = (int)nc;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.status = st->status;
+    a.timeout_ns = g_timeout_ns.load();
+    return from_cuda(fa::launch_decode_fused(tk, tv, a, d, (int)dtype, (cudaStream_t)stream));
+}
+
 FA_EXPORT const char* fa_status_string(fa_status status) {
     switch (status) {
         case FA_OK: return "FA_OK";
@@ -254,8 +325,10 @@ FA_EXPORT void fa_release_workspaces(void) {
         if (kv.second.workspaces.empty()) continue;
         if (cudaSetDevice(kv.first) != cudaSuccess) continue;
         cudaDeviceSynchronize();
-        for (auto& w : kv.second.workspaces)
+        for (auto& w : kv.second.workspaces) {
             if (w.second.ptr) cudaFree(w.second.ptr);
+            if (w.second.tickets) cudaFree(w.second.tickets);
+        }
         kv.second.workspaces.clear();
     }
     if (have_cur) cudaSetDevice(cur);

@@ -64,7 +64,43 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
     f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
-template <int D, typename T, int GP>
+// Merges n partial results (fp32 rows of D at rows + i*D, normalised, with
+// log2-domain LSEs lse[i]) into one with the LSE weights of the page's Step 2:
+// w_i = 2^(lse_i - glse), glse = log2 sum_i 2^lse_i.  128 threads; thread t < D
+// owns column t.  Returns glse; writes the row to out_f (fp32) or out_t.
+template <int D, typename T>
+__device__ float merge_partials(const float* lse, const float* rows, int n, float* red,
+                                float* out_f, T* out_t) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float mx = -INFINITY;
+    for (int i = tid; i < n; i += 128) mx = fmaxf(mx, __ldcg(lse + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+    float sm = 0.f;
+    for (int i = tid; i < n; i += 128) sm += fast_exp2(__ldcg(lse + i) - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
+    if (lane == 0) red[warp] = sm;
+    __syncthreads();
+    sm = red[0] + red[1] + red[2] + red[3];
+    __syncthreads();
+    const float glse = mx + log2f(sm);
+    if (tid < D) {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < n; ++i)
+            acc = fmaf(fast_exp2(__ldcg(lse + i) - glse), __ldcg(rows + size_t(i) * D + tid), acc);
+        if (out_f != nullptr) out_f[tid] = acc;
+        if (out_t != nullptr) out_t[tid] = static_cast<T>(acc);
+    }
+    return glse;
+}
+
+template <int D, typename T, int GP, bool FUSED>
 __global__ void __launch_bounds__(128, 3)
     decode_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
@@ -304,8 +340,60 @@ __global__ void __launch_bounds__(128, 3)
         mbar_drain_wait(kbar, uint32_t(loads - 1) & 1u, wc, FA_SITE_DRAIN);
         mbar_drain_wait(vbar, uint32_t(loads - 1) & 1u, wc, FA_SITE_DRAIN);
     }
-    // this CTA's partials are written: the merge grid may be scheduled
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if constexpr (!FUSED) {
+        // this CTA's partials are written: the merge grid may be scheduled
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    } else {
+        // Single launch (no merge kernel): the last CTA to finish a group of
+        // kDecodeMergeGroup chunks merges the group's partials; the last group
+        // merge of a (b, kv head) merges the group results into O and LSE.
+        // Tickets are reset by whoever finishes them, so they are zero again
+        // when the kernel ends.
+        __shared__ int s_last;
+        __shared__ float s_red[4];
+        // The barrier orders every thread's partial stores before thread 0's
+        // device-scope fence, which is cumulative; then the ticket.
+        if (!__syncthreads_and(ok)) return;
+        const int grp = c / kDecodeMergeGroup;
+        const int c0 = grp * kDecodeMergeGroup;
+        const int gsize = min(kDecodeMergeGroup, a.nc - c0);
+        int* t1 = a.tickets + (size_t(b) * a.Hkv + kvh) * a.ngroups + grp;
+        int* t2 = a.tickets + size_t(a.B) * a.Hkv * a.ngroups + (size_t(b) * a.Hkv + kvh);
+        if (tid == 0) {
+            __threadfence();
+            s_last = atomicAdd(t1, 1) == gsize - 1;
+            if (s_last) __threadfence();  // acquire: the others' partials are visible
+        }
+        __syncthreads();
+        if (!s_last) return;
+        for (int gi = 0; gi < g; ++gi) {
+            const size_t bh = size_t(b) * a.Hq + kvh * g + gi;
+            const size_t src = bh * a.nc + c0;
+            const size_t dst = bh * a.ngroups + grp;
+            const float glse = merge_partials<D, T>(a.lse_part + src, a.o_part + src * D, gsize,
+                                                    s_red, a.g_o + dst * D, nullptr);
+            if (tid == 0) a.g_lse[dst] = glse;
+            __syncthreads();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            *t1 = 0;
+            __threadfence();
+            s_last = atomicAdd(t2, 1) == a.ngroups - 1;
+            if (s_last) __threadfence();
+        }
+        __syncthreads();
+        if (!s_last) return;
+        for (int gi = 0; gi < g; ++gi) {
+            const size_t bh = size_t(b) * a.Hq + kvh * g + gi;
+            const float glse = merge_partials<D, T>(a.g_lse + bh * a.ngroups,
+                                                    a.g_o + bh * a.ngroups * D, a.ngroups, s_red,
+                                                    nullptr, reinterpret_cast<T*>(a.o) + bh * D);
+            if (tid == 0 && a.lse != nullptr) a.lse[bh] = glse * kLn2;
+            __syncthreads();
+        }
+        if (tid == 0) *t2 = 0;
+    }
 }
 
 // One CTA of 128 threads per (b, h) and 16 output columns: thread t owns the
@@ -376,11 +464,11 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     if (tid == 0 && blockIdx.y == 0 && a.lse != nullptr) a.lse[bh] = glse * kLn2;
 }
 
-template <int D, typename T, int GP>
+template <int D, typename T, int GP, bool FUSED = false>
 cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                          cudaStream_t stream) {
     using C = DecodeCfg<D>;
-    auto kern = decode_chunk_kernel<D, T, GP>;
+    auto kern = decode_chunk_kernel<D, T, GP, FUSED>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
@@ -411,6 +499,15 @@ cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, T>, a);
+}
+
+template <int D, typename T>
+cudaError_t launch_decode_fused_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                  cudaStream_t stream) {
+    const int g = a.Hq / a.Hkv;
+    return (g % 4 == 0)   ? launch_chunk<D, T, 4, true>(tk, tv, a, stream)
+           : (g % 2 == 0) ? launch_chunk<D, T, 2, true>(tk, tv, a, stream)
+                          : launch_chunk<D, T, 1, true>(tk, tv, a, stream);
 }
 
 __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns) {
@@ -462,6 +559,17 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
     if (d == 64)
         return dtype == 0 ? launch_decode_t<64, __half>(tk, tv, a, stream)
                           : launch_decode_t<64, __nv_bfloat16>(tk, tv, a, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_fused(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                int d, int dtype, cudaStream_t stream) {
+    if (d == 128)
+        return dtype == 0 ? launch_decode_fused_t<128, __half>(tk, tv, a, stream)
+                          : launch_decode_fused_t<128, __nv_bfloat16>(tk, tv, a, stream);
+    if (d == 64)
+        return dtype == 0 ? launch_decode_fused_t<64, __half>(tk, tv, a, stream)
+                          : launch_decode_fused_t<64, __nv_bfloat16>(tk, tv, a, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -45,6 +45,11 @@ struct DecodeArgs {
     float scale_log2;
     int* status;
     unsigned long long timeout_ns;
+    // single-launch variant only: group partials and self-resetting tickets
+    float* g_o;            // [B, Hq, ngroups, d] fp32
+    float* g_lse;          // [B, Hq, ngroups] fp32, log2 domain
+    int* tickets;          // B*Hkv*ngroups group tickets, then B*Hkv head tickets; all zero between calls
+    int ngroups;           // ceil(nc / kDecodeMergeGroup)
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -65,10 +70,15 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int d,
                           int dtype, cudaStream_t stream);
 
+// Single launch: the chunk kernel merges its own partials (two-level ticket merge).
+cudaError_t launch_decode_fused(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                int d, int dtype, cudaStream_t stream);
+
 cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cudaStream_t stream);
 
 // Geometry the host needs to build tensor maps.
 constexpr int kPrefillTile = 128;   // query rows per tile and keys per KV tile
 constexpr int kDecodeSubTile = 128; // keys per decode sub-tile
+constexpr int kDecodeMergeGroup = 32;  // chunks merged together at the first level (single launch)
 
 }  // namespace fa

@@ -110,6 +110,26 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
                     float scale, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * Split-KV decode in a single launch.  Same arguments, layouts, results and
+ * errors as fa_decode; the chunk partials are merged by the chunk kernel
+ * itself instead of a second kernel: the last CTA to finish each group of 32
+ * consecutive chunks of a (b, kv head) merges that group's partials with the
+ * LSE weights of "CUDA 实现 Flash Decoding" section 2.2 Step 2, and the last
+ * group to finish merges the group results into o and lse (the merge is
+ * associative, so the result is the same up to rounding order).  The
+ * page's section 8 lists this single launch as its fourth lever.
+ *
+ * Workspace: the same per-(device, stream) buffer as fa_decode, plus the group
+ * results (B*Hq*ceil(nc/32)*(d+1) fp32), plus B*Hkv*(ceil(nc/32)+1) int
+ * tickets that are zeroed when allocated and reset by the kernel itself; after
+ * a call that reported FA_ERR_TIMEOUT call fa_release_workspaces() before the
+ * next call on that stream.
+ */
+fa_status fa_decode_fused(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int M, int d, int chunk,
+                          float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * Split-KV decode that allocates no device memory.  The pages have no
  * counterpart: this entry point exists for callers that cannot call
  * cudaMalloc -- code running while a CUDA graph is captured, processes whose

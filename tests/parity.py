@@ -32,10 +32,10 @@ def run_prefill(q, k, v, causal, scale, stream=None):
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
-def run_decode(q, k, v, chunk, scale):
+def run_decode(q, k, v, chunk, scale, single_launch=False):
     import exact_attention_05_gb300 as fa
     torch = torch_cuda()
-    o, lse = fa.decode(q.cuda(), k.cuda(), v.cuda(), chunk, scale)
+    o, lse = fa.decode(q.cuda(), k.cuda(), v.cuda(), chunk, scale, single_launch=single_launch)
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_status() == fa.FA_OK
     return o.double().cpu().numpy(), lse.double().cpu().numpy()

@@ -32,22 +32,24 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("single", [False, True], ids=["two_kernels", "single_launch"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}_H{}x{}_M{}_d{}_{}_c{}".format(
     c[0], c[1], c[2], c[3], c[4], "f16" if c[5] == FP16 else "bf16", c[6]))
-def test_decode_parity(oracle_mod, case):
+def test_decode_parity(oracle_mod, case, single):
     B, Hq, Hkv, M, d, dtype, chunk = case
     scale = 1.0 / d ** 0.5
     q, k, v = make_inputs(B, Hq, Hkv, 1, M, d, dtype, seed=31 + M)
-    o, lse = run_decode(q, k, v, chunk, scale)
+    o, lse = run_decode(q, k, v, chunk, scale, single_launch=single)
     o_ref, lse_ref = oracle_mod.attention(bits(q), bits(k), bits(v), dtype, False, scale)
     assert_close(o, lse, o_ref, lse_ref[:, :, 0], dtype, f"decode {case}")
 
 
+@pytest.mark.parametrize("single", [False, True], ids=["two_kernels", "single_launch"])
 @pytest.mark.parametrize("name", ["decode_b1_h8_m512_f16", "decode_b2_h8_m65536_f16"])
-def test_decode_workload_full(oracle_mod, name):
+def test_decode_workload_full(oracle_mod, name, single):
     w = WORKLOADS[name]
     q, k, v = workload_inputs(w)
-    o, lse = run_decode(q, k, v, w.chunk, w.scale)
+    o, lse = run_decode(q, k, v, w.chunk, w.scale, single_launch=single)
     o_ref, lse_ref = oracle_mod.attention(bits(q), bits(k), bits(v), w.dtype, False, w.scale)
     assert_close(o, lse, o_ref, lse_ref[:, :, 0], w.dtype, name)
 
@@ -59,3 +61,16 @@ def test_decode_matches_chunked_oracle(oracle_mod):
     o, lse = run_decode(q, k, v, chunk, 0.1)
     _, _, o_ref, lse_ref = oracle_mod.decode_chunked(bits(q), bits(k), bits(v), FP16, chunk, 0.1)
     assert_close(o, lse, o_ref, lse_ref, FP16, "decode vs chunked oracle")
+
+
+def test_single_launch_tickets_reset_between_calls(oracle_mod):
+    """The single-launch decode's tickets must be zero again after every call:
+    alternate shapes (different group counts) several times on one stream."""
+    shapes = [(2, 8, 2, 5000, 128, FP16, 64), (1, 4, 4, 777, 64, BF16, 16),
+              (2, 8, 2, 5000, 128, FP16, 64)]
+    for rep in range(2):
+        for i, (B, Hq, Hkv, M, d, dtype, chunk) in enumerate(shapes):
+            q, k, v = make_inputs(B, Hq, Hkv, 1, M, d, dtype, seed=90 + i)
+            o, lse = run_decode(q, k, v, chunk, 0.1, single_launch=True)
+            o_ref, lse_ref = oracle_mod.attention(bits(q), bits(k), bits(v), dtype, False, 0.1)
+            assert_close(o, lse, o_ref, lse_ref[:, :, 0], dtype, f"rep {rep} shape {i}")
