@@ -186,94 +186,112 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t fmt = DTypeFmt<T>::value;
             constexpr uint32_t idesc_qk = instr_desc_f16(fmt, 128, 128, 0, 0);  // Q, K both K-major
             constexpr uint32_t idesc_pv = instr_desc_f16(fmt, 128, D, 0, 1);    // V is MN-major
-            auto slot_of = [](int L) { return L % C::NSLOT; };
-            auto phase_of = [](int L) { return uint32_t(L / C::NSLOT) & 1u; };
-            auto slot_addr = [&](int L) { return sbase + C::SLOT_OFF + slot_of(L) * C::TILE_BYTES; };
-            // S_i = Q_i K^T from the K tile of load L
-            auto qk = [&](int i, int L) {
-                const uint32_t qb = sbase + C::Q_OFF + i * C::TILE_BYTES;
-                const uint32_t kb = slot_addr(L);
+            // Issue must be cheap: the issuing thread shares its SMSP with two
+            // softmax warps and the tensor core executes one 128x128x16 MMA every
+            // 64 cycles, so descriptors are built once and advanced by constants
+            // (the start address sits in the low 14 bits and never carries here:
+            // shared addresses are below 256 KB), and ring slots and phases are
+            // tracked incrementally.
+            constexpr uint64_t kSlotStep = C::TILE_BYTES >> 4;
+            const uint64_t dq0 = smem_desc(sbase + C::Q_OFF, 16, 1024);
+            const uint64_t dq1 = dq0 + kSlotStep;
+            const uint64_t dk0 = smem_desc(sbase + C::SLOT_OFF, 16, 1024);         // K-major view
+            const uint64_t dv0 = smem_desc(sbase + C::SLOT_OFF, C::SUB_BYTES, 1024); // MN-major view
+            const uint32_t bar_full0 = bar(C::B_FULL), bar_empty0 = bar(C::B_EMPTY);
+            // S_i = Q_i K^T from the K tile in ring slot ks
+            auto qk = [&](int i, int ks) {
+                const uint64_t da = i ? dq1 : dq0;
+                const uint64_t db = dk0 + uint64_t(ks) * kSlotStep;
+                const uint32_t d_tmem = tmem + C::tm_s(i);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // K-major, 128-byte swizzle: k-steps of 16 elements advance 32 bytes
                     // inside a 64-column half; 8-row groups are 1024 bytes apart.
-                    const uint32_t off = (kk / 4) * C::SUB_BYTES + (kk % 4) * 32;
-                    mma_ss(tmem + C::tm_s(i), smem_desc(qb + off, 16, 1024),
-                           smem_desc(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    const uint64_t off = uint64_t((kk / 4) * C::SUB_BYTES + (kk % 4) * 32) >> 4;
+                    mma_ss(d_tmem, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::B_SFULL + i));
             };
-            // O_i (+)= P_i V from the V tile of load L
-            auto pv = [&](int i, int L, bool accumulate) {
-                const uint32_t vb = slot_addr(L);
+            // O_i (+)= P_i V from the V tile in ring slot vs
+            auto pv = [&](int i, int vs, bool accumulate) {
+                const uint64_t db = dv0 + uint64_t(vs) * kSlotStep;
+                const uint32_t d_tmem = tmem + C::tm_o(i);
+                const uint32_t a_tmem = tmem + C::tm_p(i);
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
                     // V is [key][d] = MN-major for B (N = d): 16 keys = 16 rows of 128 B;
                     // the two 64-column halves are SUB_BYTES apart (leading offset),
                     // 8-key groups 1024 bytes apart (stride offset).  P: 16 keys of
                     // 16-bit values = 8 TMEM columns.
-                    mma_ts(tmem + C::tm_o(i), tmem + C::tm_p(i) + kk * 8,
-                           smem_desc(vb + kk * 16 * 128, C::SUB_BYTES, 1024), idesc_pv,
+                    mma_ts(d_tmem, a_tmem + kk * 8, db + uint64_t(kk * 16 * 128 >> 4), idesc_pv,
                            (accumulate || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(C::B_ODONE + i));
             };
-            auto wait_full = [&](int L) -> bool {
-                if (!mbar_wait(bar(C::B_FULL + slot_of(L)), phase_of(L), wc, FA_SITE_MMA_KV))
-                    return false;
-                tc_fence_after();
-                return true;
+            auto wait_slot = [&](int slot, uint32_t phase) -> bool {
+                return mbar_wait(bar_full0 + 8u * slot, phase, wc, FA_SITE_MMA_KV);
             };
-            auto release = [&](int L) { mma_commit(bar(C::B_EMPTY + slot_of(L))); };
+            auto release = [&](int slot) { mma_commit(bar_empty0 + 8u * slot); };
 
-            bool ok = mbar_wait(bar(C::B_QFULL), 0, wc, FA_SITE_MMA_Q);
-            if (ok) tc_fence_after();
-            if (ok) ok = wait_full(0);
+            // ring positions of K_j (load 2j) and V_j (load 2j+1)
+            int ks = 0, vs = 1 % C::NSLOT;
+            uint32_t kph = 0, vph = (1 / C::NSLOT) & 1;
+            auto advance2 = [](int& slot, uint32_t& ph) {
+                slot += 2;
+                if (slot >= C::NSLOT) {
+                    slot -= C::NSLOT;
+                    ph ^= 1u;
+                }
+            };
+
+            bool ok = mbar_wait(bar(C::B_QFULL), 0, wc, FA_SITE_MMA_Q) && wait_slot(ks, kph);
             if (ok) {
-                qk(0, 0);
-                if (t1) qk(1, 0);
-                release(0);  // K0
+                tc_fence_after();
+                qk(0, ks);
+                if (t1) qk(1, ks);
+                release(ks);  // K0
             }
+            // Everything a tile's group of MMAs needs (its P, V_j and the next K
+            // tile) is waited for before the group is issued, so that PV_i(j) and
+            // QK_i(j+1) go to the tensor core back to back.
             for (int j = 0; ok && j < nt; ++j) {
-                const int LV = 2 * j + 1, LK = 2 * j + 2;
-                bool have_v = false, have_k = false;
+                int nks = ks;
+                uint32_t nkph = kph;
+                advance2(nks, nkph);  // K_{j+1}
+                const bool next_k = j + 1 < nt;  // some tile still needs K_{j+1}
+                bool have_vk = false;
                 if (j < nt0) {
-                    if (!mbar_wait(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P) || !wait_full(LV)) {
+                    if (!mbar_wait(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P) ||
+                        !wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    have_v = true;
-                    pv(0, LV, j > 0);
-                    if (!t1) release(LV);
+                    have_vk = true;
+                    pv(0, vs, j > 0);
+                    if (!t1) release(vs);
                     if (j + 1 < nt0) {
-                        if (!wait_full(LK)) {
-                            ok = false;
-                            break;
-                        }
-                        have_k = true;
-                        qk(0, LK);
-                        if (!t1) release(LK);
+                        qk(0, nks);
+                        if (!t1) release(nks);
                     }
                 }
                 if (t1) {
                     if (!mbar_wait(bar(C::B_PFULL + 1), j & 1, wc, FA_SITE_MMA_P) ||
-                        (!have_v && !wait_full(LV))) {
+                        (!have_vk && (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph))))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    pv(1, LV, j > 0);
-                    release(LV);
-                    if (j + 1 < nt) {
-                        if (!have_k && !wait_full(LK)) {
-                            ok = false;
-                            break;
-                        }
-                        qk(1, LK);
-                        release(LK);
+                    pv(1, vs, j > 0);
+                    release(vs);
+                    if (next_k) {
+                        qk(1, nks);
+                        release(nks);
                     }
                 }
+                ks = nks;
+                kph = nkph;
+                advance2(vs, vph);
             }
             // All MMAs must be complete before TMEM is released.
             mma_commit(bar(C::B_DRAIN));
