@@ -182,6 +182,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// Same contract, but polls with the non-suspending test instead of try_wait:
+// for the latency-critical roles (the MMA issuer and the softmax warps), where
+// the wake-up delay of a suspended try_wait shows up directly as idle tensor
+// core.  Costs issue slots while it spins.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                               int where) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*w.abort_flag) return false;
+            if (global_timer_ns() - t0 > w.timeout_ns) {
+                record_timeout(w.abort_flag, w.status, where);
+                return false;
+            }
+        }
+    }
+}
+
 // Same, but ignores the abort flag: used while draining in-flight copies and
 // MMAs before the CTA exits, still bounded by the timeout.
 __device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& w,

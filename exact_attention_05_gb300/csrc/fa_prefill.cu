@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(bar(C::B_ODONE + i));
             };
             auto wait_slot = [&](int slot, uint32_t phase) -> bool {
-                return mbar_wait(bar_full0 + 8u * slot, phase, wc, FA_SITE_MMA_KV);
+                return mbar_wait_spin(bar_full0 + 8u * slot, phase, wc, FA_SITE_MMA_KV);
             };
             auto release = [&](int slot) { mma_commit(bar_empty0 + 8u * slot); };
 
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
 
-            bool ok = mbar_wait(bar(C::B_QFULL), 0, wc, FA_SITE_MMA_Q) && wait_slot(ks, kph);
+            bool ok = mbar_wait_spin(bar(C::B_QFULL), 0, wc, FA_SITE_MMA_Q) && wait_slot(ks, kph);
             if (ok) {
                 tc_fence_after();
                 qk(0, ks);
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool next_k = j + 1 < nt;  // some tile still needs K_{j+1}
                 bool have_vk = false;
                 if (j < nt0) {
-                    if (!mbar_wait(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P) ||
+                    if (!mbar_wait_spin(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P) ||
                         !wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph))) {
                         ok = false;
                         break;
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (t1) {
-                    if (!mbar_wait(bar(C::B_PFULL + 1), j & 1, wc, FA_SITE_MMA_P) ||
+                    if (!mbar_wait_spin(bar(C::B_PFULL + 1), j & 1, wc, FA_SITE_MMA_P) ||
                         (!have_vk && (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph))))) {
                         ok = false;
                         break;
