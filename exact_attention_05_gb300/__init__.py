@@ -60,7 +60,8 @@ def load_library():
                 f"{LIB_PATH} is missing: build it with exact_attention_05_gb300.build.build() "
                 "(the attention path has no CPU fallback)")
         lib = ctypes.CDLL(LIB_PATH)
-        vp, fp, I, F = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        vp, fp, ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+        I, F = ctypes.c_int, ctypes.c_float
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, I, F, I, vp]
         lib.fa_fwd.restype = I
         lib.fa_decode.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
@@ -69,6 +70,11 @@ def load_library():
         lib.fa_decode_fused.restype = I
         lib.fa_decode_noalloc.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
         lib.fa_decode_noalloc.restype = I
+        lib.fa_decode_fp8.argtypes = [vp, vp, vp, fp, fp, vp, fp, I, I, I, I, I, I, F, I, vp]
+        lib.fa_decode_fp8.restype = I
+        lib.fa_decode_paged.argtypes = [vp, vp, vp, ip, ip, vp, fp, I, I, I, I, I, I, I, I, I, F,
+                                        I, vp]
+        lib.fa_decode_paged.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_get_last_device_status.argtypes = [vp]
@@ -147,6 +153,29 @@ def fa_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, st
     return _check(st, "fa_decode_noalloc") if check else st
 
 
+def fa_decode_fp8(q, k8, v8, k_scale, v_scale, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype,
+                  stream=None, check=True) -> int:
+    """Split-KV decode over e4m3 K/V bytes with fp32 per-kv-head scales."""
+    st = load_library().fa_decode_fp8(_ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale),
+                                      _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv), int(M),
+                                      int(d), int(chunk), float(scale), int(dtype),
+                                      _stream(stream))
+    return _check(st, "fa_decode_fp8") if check else st
+
+
+def fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, max_seq_len,
+                    num_pages, page_size, max_pages_per_seq, d, chunk, scale, dtype, stream=None,
+                    check=True) -> int:
+    """Split-KV decode over a paged K/V cache [num_pages, page_size, Hkv, d]
+    addressed through block_table [B, max_pages_per_seq] and seq_lens [B]."""
+    st = load_library().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                        _ptr(seq_lens), _ptr(o), _ptr(lse), int(B), int(Hq),
+                                        int(Hkv), int(max_seq_len), int(num_pages),
+                                        int(page_size), int(max_pages_per_seq), int(d),
+                                        int(chunk), float(scale), int(dtype), _stream(stream))
+    return _check(st, "fa_decode_paged") if check else st
+
+
 def fa_get_last_device_status(stream=None) -> int:
     return load_library().fa_get_last_device_status(_stream(stream))
 
@@ -209,4 +238,56 @@ def decode(q, k, v, chunk: int, scale: float, out=None, lse=None, with_lse=True,
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     fn = fa_decode_fused if single_launch else fa_decode
     fn(q, k, v, out, lse, B, Hq, Hkv, M, d, chunk, scale, _dtype_code(q), stream)
+    return out, lse
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, chunk: int, scale: float, out=None, lse=None,
+               with_lse=True, stream=None):
+    """Split-KV decode of q [B,1,Hq,d] against e4m3 k8/v8 [B,M,Hkv,d] (torch.uint8
+    or torch.float8_e4m3fn) with fp32 scales [Hkv]: K = k_scale[h] * k8, V = v_scale[h] * v8."""
+    import torch
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes q of shape [B, 1, Hq, d]")
+    _, M, Hkv, _ = k8.shape
+    for t in (k8, v8):
+        if t.element_size() != 1:
+            raise TypeError("k8 and v8 hold one byte per element")
+    for t in (q, k8, v8, k_scale, v_scale):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("scales are float32")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    fa_decode_fp8(q, k8, v8, k_scale, v_scale, out, lse, B, Hq, Hkv, M, d, chunk, scale,
+                  _dtype_code(q), stream)
+    return out, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, chunk: int,
+                 scale: float, out=None, lse=None, with_lse=True, stream=None):
+    """Split-KV decode of q [B,1,Hq,d] against a paged cache k_cache/v_cache
+    [num_pages, page_size, Hkv, d] through block_table [B, max_pages_per_seq]
+    and seq_lens [B] (both int32 on the device)."""
+    import torch
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes q of shape [B, 1, Hq, d]")
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    for t in (block_table, seq_lens):
+        if t.dtype != torch.int32:
+            raise TypeError("block_table and seq_lens are int32")
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, out, lse, B, Hq, Hkv, max_seq_len,
+                    num_pages, page_size, block_table.shape[1], d, chunk, scale, _dtype_code(q),
+                    stream)
     return out, lse

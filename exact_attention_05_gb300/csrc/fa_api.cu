@@ -168,6 +168,34 @@ fa_status tickets(DeviceState* st, cudaStream_t stream, size_t count, int** out)
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// Workspace and the common fields of a two-kernel decode launch over M keys.
+fa_status decode_setup(DeviceState* st, cudaStream_t stream, const void* q, void* o, float* lse,
+                       int B, int Hq, int Hkv, int M, int d, int chunk, float scale,
+                       fa::DecodeArgs* a) {
+    const int nc = (int)(((long long)M + chunk - 1) / chunk);
+    const size_t part_elems = (size_t)B * Hq * nc * d;
+    const size_t bytes = (part_elems + (size_t)B * Hq * nc) * sizeof(float);
+    void* ws = nullptr;
+    const fa_status s = workspace(st, stream, bytes, &ws);
+    if (s != FA_OK) return s;
+    *a = fa::DecodeArgs{};
+    a->q = q;
+    a->o = o;
+    a->lse = lse;
+    a->o_part = static_cast<float*>(ws);
+    a->lse_part = static_cast<float*>(ws) + part_elems;
+    a->B = B;
+    a->Hq = Hq;
+    a->Hkv = Hkv;
+    a->M = M;
+    a->chunk = chunk;
+    a->nc = nc;
+    a->scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a->status = st->status;
+    a->timeout_ns = g_timeout_ns.load();
+    return FA_OK;
+}
+
 }  // namespace
 
 FA_EXPORT fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -276,6 +304,65 @@ FA_EXPORT fa_status fa_decode_fused(const void* q, const void* k, const void* v,
     a.status = st->status;
     a.timeout_ns = g_timeout_ns.load();
     return from_cuda(fa::launch_decode_fused(tk, tv, a, d, (int)dtype, (cudaStream_t)stream));
+}
+
+FA_EXPORT fa_status fa_decode_fp8(const void* q, const void* k8, const void* v8,
+                                  const float* k_scale, const float* v_scale, void* o, float* lse,
+                                  int B, int Hq, int Hkv, int M, int d, int chunk, float scale,
+                                  fa_dtype dtype, fa_stream_t stream) {
+    fa_status s = check_args(q, k8, v8, o, lse, B, Hq, Hkv, 1, M, d, scale, (int)dtype);
+    if (s != FA_OK) return s;
+    if (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+        return FA_ERR_INVALID_ARG;
+    if (chunk <= 0) return FA_ERR_INVALID_ARG;
+    if (((long long)M + chunk - 1) / chunk * B * Hkv > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != FA_OK) return s;
+    fa::DecodeArgs a;
+    if ((s = decode_setup(st, (cudaStream_t)stream, q, o, lse, B, Hq, Hkv, M, d, chunk, scale, &a)) !=
+        FA_OK)
+        return s;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    CUtensorMap tk, tv;
+    if (!fa::encode_decode_maps_fp8(g_encode, k8, v8, d, Hkv, M, B, &tk, &tv)) return FA_ERR_CUDA;
+    return from_cuda(fa::launch_decode_fp8(tk, tv, a, d, (int)dtype, (cudaStream_t)stream));
+}
+
+FA_EXPORT fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                    const int* block_table, const int* seq_lens, void* o,
+                                    float* lse, int B, int Hq, int Hkv, int max_seq_len,
+                                    int num_pages, int page_size, int max_pages_per_seq, int d,
+                                    int chunk, float scale, fa_dtype dtype, fa_stream_t stream) {
+    fa_status s = check_args(q, k_cache, v_cache, o, lse, B, Hq, Hkv, 1, max_seq_len, d, scale,
+                             (int)dtype);
+    if (s != FA_OK) return s;
+    if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return FA_ERR_INVALID_ARG;
+    if (num_pages <= 0 || max_pages_per_seq <= 0) return FA_ERR_INVALID_ARG;
+    if (page_size < 8 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
+        return FA_ERR_INVALID_ARG;
+    const int rows = page_size < fa::kDecodeSubTile ? page_size : fa::kDecodeSubTile;
+    if (chunk <= 0 || chunk % rows != 0) return FA_ERR_INVALID_ARG;
+    if ((long long)max_pages_per_seq * page_size < max_seq_len) return FA_ERR_INVALID_ARG;
+    if ((uint64_t)num_pages * page_size * Hkv * d >= kMaxElements) return FA_ERR_INVALID_ARG;
+    if (((long long)max_seq_len + chunk - 1) / chunk * B * Hkv > 0x7fffffffLL)
+        return FA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != FA_OK) return s;
+    fa::DecodeArgs a;
+    if ((s = decode_setup(st, (cudaStream_t)stream, q, o, lse, B, Hq, Hkv, max_seq_len, d, chunk,
+                          scale, &a)) != FA_OK)
+        return s;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.page = page_size;
+    a.max_pages = max_pages_per_seq;
+    CUtensorMap tk, tv;
+    if (!fa::encode_decode_maps_paged(g_encode, k_cache, v_cache, (int)dtype, d, Hkv, page_size,
+                                      num_pages, &tk, &tv))
+        return FA_ERR_CUDA;
+    return from_cuda(fa::launch_decode_paged(tk, tv, a, d, (int)dtype, (cudaStream_t)stream));
 }
 
 FA_EXPORT const char* fa_status_string(fa_status status) {

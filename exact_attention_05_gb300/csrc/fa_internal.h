@@ -45,6 +45,16 @@ struct DecodeArgs {
     float scale_log2;
     int* status;
     unsigned long long timeout_ns;
+    // e4m3 K/V only: per-kv-head dequantisation scales [Hkv] (K = k8 * k_scale)
+    const float* k_scale;
+    const float* v_scale;
+    // paged K/V only: cache [num_pages, page, Hkv, d], block_table [B, max_pages]
+    // (int32 page ids), seq_lens [B] (keys of each batch, <= M); M is the
+    // largest sequence length and sets nc
+    const int* block_table;
+    const int* seq_lens;
+    int page;
+    int max_pages;
     // single-launch variant only: group partials and self-resetting tickets
     float* g_o;            // [B, Hq, ngroups, d] fp32
     float* g_lse;          // [B, Hq, ngroups] fp32, log2 domain
@@ -69,6 +79,18 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
 
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int d,
                           int dtype, cudaStream_t stream);
+
+// e4m3 K/V with per-kv-head scales (q, o of `dtype`).
+bool encode_decode_maps_fp8(EncodeTiledFn enc, const void* k8, const void* v8, int d, int Hkv,
+                            int M, int B, CUtensorMap* tk, CUtensorMap* tv);
+cudaError_t launch_decode_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                              int d, int dtype, cudaStream_t stream);
+
+// Paged K/V cache [num_pages, page, Hkv, d] addressed through a block table.
+bool encode_decode_maps_paged(EncodeTiledFn enc, const void* kc, const void* vc, int dtype, int d,
+                              int Hkv, int page, int num_pages, CUtensorMap* tk, CUtensorMap* tv);
+cudaError_t launch_decode_paged(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                int d, int dtype, cudaStream_t stream);
 
 // Single launch: the chunk kernel merges its own partials (two-level ticket merge).
 cudaError_t launch_decode_fused(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,

@@ -12,7 +12,22 @@ workload additionally picks exactly floor(1% of B*M*Hkv) key rows -- a row is
 one (b, m, h_kv) d-vector -- with a ``randperm`` drawn from the same generator
 after V, and multiplies them by 8 in float32 before rounding.
 
-Layouts: q/o [B, N, Hq, d]; k/v [B, M, Hkv, d]; decode q/o [B, 1, Hq, d].
+FP8 K/V workloads (``kv="e4m3"``): K and V are drawn as above in float32 and
+quantised per kv head the way a serving stack writes an FP8 cache: scale_h =
+amax over that head's K (or V) values / 448 (the largest finite e4m3 value),
+bytes = e4m3(x / scale_h) by torch's round-to-nearest-even cast, clamped to
++-448 first.  The attention kernels never see the float32 values, only the
+bytes and the scales.
+
+Paged workloads (``page > 0``): the contiguous K/V of a workload are cut into
+pages of ``page`` keys and scattered to a random permutation of a pool of
+pages (``randperm`` from the workload's generator, drawn after K and V); the
+pool's unused pages, and the tail of a sequence's last page, hold N(0, 1)
+noise so that a wrong gather cannot go unnoticed.  block_table [B,
+pages_per_seq] int32 lists each sequence's pages in key order.
+
+Layouts: q/o [B, N, Hq, d]; k/v [B, M, Hkv, d]; decode q/o [B, 1, Hq, d];
+paged k/v cache [num_pages, page, Hkv, d].
 """
 from __future__ import annotations
 
@@ -44,6 +59,8 @@ class Workload:
     seed: int
     chunk: int = 0       # decode only
     peaky_frac: float = 0.0
+    kv: str = "16bit"    # decode K/V format: "16bit" (dtype) or "e4m3"
+    page: int = 0        # decode: keys per page of a paged cache (0 = contiguous K/V)
     note: str = field(default="", compare=False)
 
     @property
@@ -55,10 +72,15 @@ class Workload:
     @property
     def decode_bytes(self) -> int:
         """Algorithmic HBM bytes of one decode call: K and V once per kv head, plus q and o."""
-        esz = 2
+        esz = 1 if self.kv == "e4m3" else 2
         kv = 2 * self.B * self.Hkv * self.M * self.d * esz
-        qo = 2 * self.B * self.Hq * self.d * esz
-        return kv + qo
+        qo = 2 * self.B * self.Hq * self.d * 2
+        extra = 0
+        if self.kv == "e4m3":
+            extra += 2 * self.Hkv * 4                       # k_scale, v_scale
+        if self.page > 0:
+            extra += self.B * (-(-self.M // self.page)) * 4 + self.B * 4  # block table, seq_lens
+        return kv + qo + extra
 
 
 INV_SQRT_64 = 1.0 / math.sqrt(64.0)
@@ -85,7 +107,74 @@ WORKLOADS = {
     "decode_b1_h8_m512_f16": Workload(
         "decode_b1_h8_m512_f16", "decode", 1, 8, 8, 1, 512, 128, FP16, False,
         INV_SQRT_128, 1005, chunk=128, note="split-KV decode, small case"),
+    "decode_fp8_b2_h8_m65536_f16": Workload(
+        "decode_fp8_b2_h8_m65536_f16", "decode", 2, 8, 8, 1, 65536, 128, FP16, False,
+        INV_SQRT_128, 1006, chunk=128, kv="e4m3",
+        note="split-KV decode over e4m3 K/V with per-kv-head scales, chunk 128"),
+    "decode_paged_b2_h8_m65536_p16_f16": Workload(
+        "decode_paged_b2_h8_m65536_p16_f16", "decode", 2, 8, 8, 1, 65536, 128, FP16, False,
+        INV_SQRT_128, 1007, chunk=128, page=16,
+        note="split-KV decode over a paged cache, 16-key pages in shuffled order, chunk 128"),
 }
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-kv-head e4m3 bytes and fp32 scales of a float32 [B, M, Hkv, d] tensor:
+    returns (uint8 [B, M, Hkv, d], float32 [Hkv])."""
+    Hkv = x.shape[2]
+    amax = x.abs().permute(2, 0, 1, 3).reshape(Hkv, -1).amax(dim=1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    y = (x / scale.view(1, 1, Hkv, 1)).clamp(-E4M3_MAX, E4M3_MAX)
+    return y.to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), scale.contiguous()
+
+
+def make_fp8_decode_inputs(B, Hq, Hkv, M, d, dtype, seed):
+    """q [B,1,Hq,d] of the 16-bit dtype; k8, v8 uint8 [B,M,Hkv,d]; k_scale, v_scale [Hkv]."""
+    g = torch.Generator().manual_seed(int(seed))
+    q = torch.randn((B, 1, Hq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, M, Hkv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, M, Hkv, d), generator=g, dtype=torch.float32)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    return q.to(TORCH_DTYPE[dtype]), k8, v8, ks, vs
+
+
+def make_paged(k: torch.Tensor, v: torch.Tensor, page: int, seed: int, extra_pages: int = 0):
+    """Scatters contiguous k/v [B, M, Hkv, d] into a shuffled pool of pages.
+    Returns (k_cache, v_cache [num_pages, page, Hkv, d], block_table int32
+    [B, ceil(M / page)])."""
+    B, M, Hkv, d = k.shape
+    per_seq = -(-M // page)
+    num_pages = B * per_seq + extra_pages
+    g = torch.Generator().manual_seed(int(seed))
+    perm = torch.randperm(num_pages, generator=g)[:B * per_seq].view(B, per_seq)
+    caches = []
+    for x in (k, v):
+        pool = torch.randn((num_pages, page, Hkv, d), generator=g, dtype=torch.float32).to(x.dtype)
+        pad = torch.randn((B, per_seq * page, Hkv, d), generator=g, dtype=torch.float32).to(x.dtype)
+        pad[:, :M] = x
+        pool[perm.reshape(-1)] = pad.view(B * per_seq, page, Hkv, d)
+        caches.append(pool.contiguous())
+    return caches[0], caches[1], perm.to(torch.int32).contiguous()
+
+
+def workload_decode_inputs(w: Workload):
+    """All host tensors of a decode workload, by name: q, k, v (contiguous, the
+    16-bit or e4m3 bytes), k_scale/v_scale (e4m3), k_cache, v_cache,
+    block_table, seq_lens (paged)."""
+    if w.kv == "e4m3":
+        q, k8, v8, ks, vs = make_fp8_decode_inputs(w.B, w.Hq, w.Hkv, w.M, w.d, w.dtype, w.seed)
+        out = {"q": q, "k": k8, "v": v8, "k_scale": ks, "v_scale": vs}
+    else:
+        q, k, v = make_inputs(w.B, w.Hq, w.Hkv, 1, w.M, w.d, w.dtype, w.seed)
+        out = {"q": q, "k": k, "v": v}
+    if w.page > 0:
+        kc, vc, bt = make_paged(out["k"], out["v"], w.page, w.seed + 1)
+        out.update(k_cache=kc, v_cache=vc, block_table=bt,
+                   seq_lens=torch.full((w.B,), w.M, dtype=torch.int32))
+    return out
 
 
 def make_inputs(B, Hq, Hkv, N, M, d, dtype, seed, peaky_frac=0.0):

@@ -159,6 +159,66 @@ fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int M, int d, int chunk,
                             float scale, fa_dtype dtype, fa_stream_t stream);
 
+/*
+ * Split-KV decode over an FP8 (e4m3) K/V cache with one fp32 scale per kv
+ * head.  FP8 and INT8/INT4 KV quantisation are named as the next memory-side
+ * step in the closing "TODO" section of "[CUDA 优化实战] fmha sm120 : 超越
+ * torch.sdpa(flash-attention-2)", and as lever 1 (the only lever that halves
+ * the bytes) in section 8 of "CUDA 实现 Flash Decoding：解码阶段并行度重建与
+ * 性能剖析".  This is not exact attention over the original 16-bit K/V: it is
+ * exact attention over the dequantised cache
+ *     K[b][j][h][:] = k_scale[h] * e4m3(k8[b][j][h][:]),
+ *     V[b][j][h][:] = v_scale[h] * e4m3(v8[b][j][h][:]),
+ * computed like fa_decode (same chunks, partials and merge).
+ *
+ *   q, o, lse   as fa_decode; q and o are fp16 or bf16 (`dtype`).
+ *   k8, v8      device, [B, M, Hkv, d] bytes, each an OCP e4m3 value (bias 7,
+ *               no infinities, 0x7f/0xff are NaN); 16-byte aligned.
+ *   k_scale,    device, Hkv fp32 each, finite; the kernel applies k_scale once
+ *   v_scale     per score and v_scale once per output row.
+ *   others      as fa_decode.
+ * Errors: as fa_decode, plus FA_ERR_INVALID_ARG for a NULL scale pointer or
+ * one not 4-byte aligned.  The workspace is fa_decode's.
+ */
+fa_status fa_decode_fp8(const void* q, const void* k8, const void* v8, const float* k_scale,
+                        const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int M,
+                        int d, int chunk, float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Split-KV decode over a paged K/V cache addressed through a block table, the
+ * layout paged attention needs to plug into an inference server (the closing
+ * "TODO" section of "[CUDA 优化实战] fmha sm120 : 超越
+ * torch.sdpa(flash-attention-2)", "attention with kv cache block").  Key j of
+ * sequence b is row j % page_size of page block_table[b][j / page_size]; the
+ * result is fa_decode's on the gathered K/V of the first seq_lens[b] keys.
+ *
+ *   q, o, lse          as fa_decode (one query row per (b, h)).
+ *   k_cache, v_cache   device, [num_pages, page_size, Hkv, d] of `dtype`,
+ *                      16-byte aligned.
+ *   block_table        device int32 [B, max_pages_per_seq], row-major.  Every
+ *                      entry that covers a key below seq_lens[b] must lie in
+ *                      [0, num_pages); the library cannot check device data,
+ *                      and an entry outside that range reads its rows as
+ *                      zeros (the copy engine's bounds), never out of bounds.
+ *   seq_lens           device int32 [B]: keys of sequence b, taken as
+ *                      min(seq_lens[b], max_seq_len); 0 (or negative) gives
+ *                      o = 0 and lse = -inf for that sequence.
+ *   max_seq_len        upper bound of seq_lens (sizes the chunk grid); > 0.
+ *   page_size          a power of two, 8 <= page_size <= 65536.
+ *   max_pages_per_seq  >= ceil(max_seq_len / page_size).
+ *   chunk              keys per chunk, a multiple of min(page_size, 128), so
+ *                      that every copy of keys starts on a page boundary.
+ * Errors: FA_ERR_INVALID_ARG for NULL or misaligned pointers, non-positive
+ * sizes, a page size or chunk outside the rules above, or Hq % Hkv != 0;
+ * FA_ERR_UNSUPPORTED as fa_decode.  Workspace: fa_decode's, sized with
+ * M = max_seq_len.
+ */
+fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                          const int* block_table, const int* seq_lens, void* o, float* lse, int B,
+                          int Hq, int Hkv, int max_seq_len, int num_pages, int page_size,
+                          int max_pages_per_seq, int d, int chunk, float scale, fa_dtype dtype,
+                          fa_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(fa_status status);
 

@@ -13,7 +13,11 @@ Definitions followed (see ``oracle.c`` for the passage each one restates):
 softmax attention with materialised S and P ("[CUDA 优化实战] fmha sm120",
 section 1), top-left causal mask and GQA head mapping (same page, section 2),
 natural-log LSE of the scaled logits and the chunk-partial + LSE-weighted
-merge of split-KV decoding ("CUDA 实现 Flash Decoding", section 2.2).
+merge of split-KV decoding ("CUDA 实现 Flash Decoding", section 2.2); the
+OCP E4M3 decoding of an FP8 K/V cache and the block-table gather of a paged
+cache (the fmha sm120 page's closing "TODO" section; lever 1 of the Flash
+Decoding page's section 8).  The e4m3 functions take the raw bytes
+(``numpy.uint8``) and fp32 per-kv-head scales.
 """
 from __future__ import annotations
 
@@ -75,6 +79,17 @@ def _load():
         lib.oracle_decode_chunked.argtypes = [u16p, u16p, u16p, I, I, I, I, I, I, I, D,
                                               f64p, f64p, f64p, f64p]
         lib.oracle_decode_chunked.restype = I
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = D
+        lib.oracle_decode_fp8.argtypes = [u16p, u8p, u8p, f32p, f32p, I, I, I, I, I, I, D,
+                                          f64p, f64p]
+        lib.oracle_decode_fp8.restype = I
+        lib.oracle_decode_paged.argtypes = [u16p, u16p, u16p, i32p, i32p, I, I, I, I, I, I, I,
+                                            I, I, D, f64p, f64p]
+        lib.oracle_decode_paged.restype = I
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = I
         lib.oracle_set_num_threads.argtypes = [I]
@@ -182,3 +197,68 @@ def decode_chunked(q, k, v, dtype, chunk, scale):
     if rc != 0:
         raise ValueError("oracle_decode_chunked rejected its arguments")
     return op, lp, o, lse
+
+
+def e4m3(bits: np.ndarray) -> np.ndarray:
+    """Exact fp64 value of each e4m3 byte (the oracle's own decoder)."""
+    lib = _load()
+    flat = np.ascontiguousarray(bits, dtype=np.uint8).ravel()
+    return np.array([lib.oracle_e4m3_to_double(int(x)) for x in flat],
+                    dtype=np.float64).reshape(np.shape(bits))
+
+
+def _typed(a, dt, ct, what):
+    a = np.ascontiguousarray(a)
+    if a.dtype != dt:
+        raise TypeError(f"{what} must be {np.dtype(dt).name}")
+    return a, a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, dtype, scale):
+    """Decode of q [B,1,Hq,d] (uint16 bits) over e4m3 bytes k8/v8 [B,M,Hkv,d]
+    (uint8) with float32 scales [Hkv].  Returns (O [B,1,Hq,d], LSE [B,Hq])."""
+    lib = _load()
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes a single query row per head")
+    _, M, Hkv, _ = k8.shape
+    q, qp = _u16(q)
+    k8, kp = _typed(k8, np.uint8, ctypes.c_uint8, "k8")
+    v8, vp = _typed(v8, np.uint8, ctypes.c_uint8, "v8")
+    ks, ksp = _typed(k_scale, np.float32, ctypes.c_float, "k_scale")
+    vs, vsp = _typed(v_scale, np.float32, ctypes.c_float, "v_scale")
+    if ks.shape != (Hkv,) or vs.shape != (Hkv,):
+        raise ValueError("scales are [Hkv]")
+    o = np.zeros((B, 1, Hq, d), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib.oracle_decode_fp8(qp, kp, vp, ksp, vsp, int(dtype), B, Hq, Hkv, M, d, float(scale),
+                               _f64(o), _f64(lse))
+    if rc != 0:
+        raise ValueError("oracle_decode_fp8 rejected its arguments")
+    return o, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, dtype, max_seq_len, scale):
+    """Decode of q [B,1,Hq,d] over a paged cache k/v [num_pages, page, Hkv, d]
+    (uint16 bits) through block_table [B, max_pages] and seq_lens [B] (int32).
+    Returns (O [B,1,Hq,d], LSE [B,Hq]); an empty sequence gives O = 0, LSE = -inf."""
+    lib = _load()
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes a single query row per head")
+    num_pages, page, Hkv, _ = k_cache.shape
+    q, qp = _u16(q)
+    kc, kp = _u16(k_cache)
+    vc, vp = _u16(v_cache)
+    bt, btp = _typed(block_table, np.int32, ctypes.c_int32, "block_table")
+    sl, slp = _typed(seq_lens, np.int32, ctypes.c_int32, "seq_lens")
+    if bt.ndim != 2 or bt.shape[0] != B or sl.shape != (B,):
+        raise ValueError("block_table is [B, max_pages], seq_lens [B]")
+    o = np.zeros((B, 1, Hq, d), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib.oracle_decode_paged(qp, kp, vp, btp, slp, int(dtype), B, Hq, Hkv, int(max_seq_len),
+                                 num_pages, page, bt.shape[1], d, float(scale), _f64(o),
+                                 _f64(lse))
+    if rc != 0:
+        raise ValueError("oracle_decode_paged rejected its arguments")
+    return o, lse

@@ -33,8 +33,15 @@
  *   log sum_c exp(lse_c - m), w_c = exp(lse_c - global_lse), O = sum_c w_c
  *   O_c).
  *
- * Layouts: q, o [B, N, Hq, d]; k, v [B, M, Hkv, d]; lse [B, Hq, N]; all
- * contiguous.  dtype 0 = IEEE fp16, 1 = bfloat16.
+ *   FP8 K/V decode: attention over K = k_scale[h] * e4m3(k8), V likewise,
+ *   with the OCP E4M3 format decoded from its definition.
+ *
+ *   paged K/V decode: key j of sequence b gathered from page
+ *   block_table[b][j / page], row j % page, for j < seq_lens[b].
+ *
+ * Layouts: q, o [B, N, Hq, d]; k, v [B, M, Hkv, d]; lse [B, Hq, N]; paged
+ * caches [num_pages, page, Hkv, d]; all contiguous.  dtype 0 = IEEE fp16,
+ * 1 = bfloat16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -311,6 +318,148 @@ int oracle_decode_chunked(const uint16_t* q, const uint16_t* k, const uint16_t* 
         free(prow);
         free(Oc);
         free(Lc);
+    }
+    return failed ? -1 : 0;
+}
+
+/* ---- FP8 (e4m3) K/V --------------------------------------------------------- */
+
+/*
+ * OCP 8-bit floating point E4M3 (the format the FP8 KV-cache quantisation of
+ * the fmha sm120 page's closing "TODO" section and lever 1 of the Flash
+ * Decoding page's section 8 store): 1 sign bit, 4 exponent bits (bias 7),
+ * 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); there are no
+ * infinities, and exponent 15 with mantissa 7 is NaN (so the largest finite
+ * value is 1.75 * 2^8 = 448).
+ */
+double oracle_e4m3_to_double(uint8_t bits) {
+    const int sign = (bits >> 7) & 1;
+    const int expo = (bits >> 3) & 0xf;
+    const int mant = bits & 0x7;
+    double mag;
+    if (expo == 0xf && mant == 0x7)
+        mag = NAN;
+    else if (expo == 0)
+        mag = ldexp((double)mant, -9);            /* mant/8 * 2^(1-7) */
+    else
+        mag = ldexp((double)(8 + mant), expo - 10); /* (1 + mant/8) * 2^(expo-7) */
+    return sign ? -mag : mag;
+}
+
+/*
+ * Decode against an e4m3 K/V cache: exact attention of each query row
+ * q [B,1,Hq,d] (16-bit dtype) over the dequantised cache
+ *     K[b][j][h] = k_scale[h] * e4m3(k8[b][j][h]),  V likewise with v_scale,
+ * k8/v8 [B,M,Hkv,d] bytes, scales [Hkv].  o [B,Hq,d], lse [B,Hq] (natural
+ * log); either may be NULL.  The split into chunks and their merge reproduce
+ * this result exactly up to rounding order, so the definition is the oracle.
+ */
+int oracle_decode_fp8(const uint16_t* q, const uint8_t* k8, const uint8_t* v8,
+                      const float* k_scale, const float* v_scale, int dtype, int B, int Hq,
+                      int Hkv, int M, int d, double scale, double* o, double* lse) {
+    if (check_shape(B, Hq, Hkv, 1, M, d)) return -1;
+    const int g = Hq / Hkv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * Hq; ++bh) {
+        const int b = bh / Hq, h = bh % Hq, kh = h / g;
+        double* K = malloc(sizeof(double) * (size_t)M * d);
+        double* V = malloc(sizeof(double) * (size_t)M * d);
+        double* qrow = malloc(sizeof(double) * (size_t)d);
+        double* srow = malloc(sizeof(double) * (size_t)M);
+        double* prow = malloc(sizeof(double) * (size_t)M);
+        double* orow = malloc(sizeof(double) * (size_t)d);
+        if (!K || !V || !qrow || !srow || !prow || !orow) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+            const double ks = (double)k_scale[kh], vs = (double)v_scale[kh];
+            for (int j = 0; j < M; ++j) {
+                const size_t src = (((size_t)b * M + j) * Hkv + kh) * (size_t)d;
+                for (int t = 0; t < d; ++t) {
+                    K[(size_t)j * d + t] = ks * oracle_e4m3_to_double(k8[src + t]);
+                    V[(size_t)j * d + t] = vs * oracle_e4m3_to_double(v8[src + t]);
+                }
+            }
+            decode_array(q + ((size_t)b * Hq + h) * (size_t)d, qrow, (size_t)d, dtype);
+            double l;
+            attend_row(qrow, K, V, M, d, scale, srow, prow, orow, &l);
+            if (o) memcpy(o + (size_t)bh * d, orow, sizeof(double) * (size_t)d);
+            if (lse) lse[bh] = l;
+        }
+        free(K);
+        free(V);
+        free(qrow);
+        free(srow);
+        free(prow);
+        free(orow);
+    }
+    return failed ? -1 : 0;
+}
+
+/* ---- paged K/V cache ------------------------------------------------------- */
+
+/*
+ * Decode against a paged K/V cache (the "attention with kv cache block" item
+ * of the fmha sm120 page's closing "TODO" section): key j of sequence b is row
+ * j % page of page block_table[b * max_pages + j / page] of the caches
+ * kc/vc [num_pages, page, Hkv, d]; sequence b has L_b = min(seq_lens[b], M)
+ * keys.  Gathers those rows, then takes the definition as above.  L_b <= 0
+ * gives o = 0 and lse = -inf (an empty softmax).  Returns -1 on a bad shape,
+ * an allocation failure or a block-table entry outside [0, num_pages) for a
+ * key below L_b.
+ */
+int oracle_decode_paged(const uint16_t* q, const uint16_t* kc, const uint16_t* vc,
+                        const int32_t* block_table, const int32_t* seq_lens, int dtype, int B,
+                        int Hq, int Hkv, int M, int num_pages, int page, int max_pages, int d,
+                        double scale, double* o, double* lse) {
+    if (check_shape(B, Hq, Hkv, 1, M, d) || num_pages <= 0 || page <= 0 || max_pages <= 0)
+        return -1;
+    if ((long long)max_pages * page < M) return -1;
+    const int g = Hq / Hkv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * Hq; ++bh) {
+        const int b = bh / Hq, h = bh % Hq, kh = h / g;
+        const int L = seq_lens[b] < M ? seq_lens[b] : M;
+        const int n = L > 0 ? L : 1;
+        double* K = malloc(sizeof(double) * (size_t)n * d);
+        double* V = malloc(sizeof(double) * (size_t)n * d);
+        double* qrow = malloc(sizeof(double) * (size_t)d);
+        double* srow = malloc(sizeof(double) * (size_t)n);
+        double* prow = malloc(sizeof(double) * (size_t)n);
+        double* orow = malloc(sizeof(double) * (size_t)d);
+        int bad = !K || !V || !qrow || !srow || !prow || !orow;
+        for (int j = 0; j < L && !bad; ++j) {
+            const int pg = block_table[(size_t)b * max_pages + j / page];
+            if (pg < 0 || pg >= num_pages) {
+                bad = 1;
+                break;
+            }
+            const size_t src = (((size_t)pg * page + j % page) * Hkv + kh) * (size_t)d;
+            decode_array(kc + src, K + (size_t)j * d, (size_t)d, dtype);
+            decode_array(vc + src, V + (size_t)j * d, (size_t)d, dtype);
+        }
+        if (bad) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+            double l = -INFINITY;
+            if (L > 0) {
+                decode_array(q + ((size_t)b * Hq + h) * (size_t)d, qrow, (size_t)d, dtype);
+                attend_row(qrow, K, V, L, d, scale, srow, prow, orow, &l);
+            } else {
+                for (int t = 0; t < d; ++t) orow[t] = 0.0;
+            }
+            if (o) memcpy(o + (size_t)bh * d, orow, sizeof(double) * (size_t)d);
+            if (lse) lse[bh] = l;
+        }
+        free(K);
+        free(V);
+        free(qrow);
+        free(srow);
+        free(prow);
+        free(orow);
     }
     return failed ? -1 : 0;
 }

@@ -61,7 +61,26 @@ def dec(**kw):
                         args["scale"], args["dtype"], stream=0, check=False)
 
 
-@pytest.mark.parametrize("call", [fwd, dec])
+def dec8(**kw):
+    args = dict(q=GOOD, k=GOOD, v=GOOD, ks=GOOD, vs=GOOD, o=GOOD, lse=None, B=1, Hq=2, Hkv=2,
+                M=128, d=128, chunk=128, scale=0.1, dtype=0)
+    args.update(kw)
+    return fa.fa_decode_fp8(args["q"], args["k"], args["v"], args["ks"], args["vs"], args["o"],
+                            args["lse"], args["B"], args["Hq"], args["Hkv"], args["M"], args["d"],
+                            args["chunk"], args["scale"], args["dtype"], stream=0, check=False)
+
+
+def decp(**kw):
+    args = dict(q=GOOD, k=GOOD, v=GOOD, bt=GOOD, sl=GOOD, o=GOOD, lse=None, B=1, Hq=2, Hkv=2,
+                M=128, num_pages=8, page=16, max_pages=8, d=128, chunk=128, scale=0.1, dtype=0)
+    args.update(kw)
+    return fa.fa_decode_paged(args["q"], args["k"], args["v"], args["bt"], args["sl"], args["o"],
+                              args["lse"], args["B"], args["Hq"], args["Hkv"], args["M"],
+                              args["num_pages"], args["page"], args["max_pages"], args["d"],
+                              args["chunk"], args["scale"], args["dtype"], stream=0, check=False)
+
+
+@pytest.mark.parametrize("call", [fwd, dec, dec8, decp])
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), fa.FA_ERR_INVALID_ARG),
     (dict(k=None), fa.FA_ERR_INVALID_ARG),
@@ -103,6 +122,26 @@ def test_invalid_forward_only_arguments(lib, kw):
                                                                         M=1, d=64)])
 def test_invalid_decode_only_arguments(lib, kw):
     assert dec(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(ks=None), dict(vs=None), dict(ks=GOOD + 2),
+                                dict(vs=GOOD + 1), dict(chunk=0),
+                                dict(B=1 << 16, Hkv=1 << 16, Hq=1 << 16, M=1 << 20, d=64)])
+def test_invalid_fp8_decode_arguments(lib, kw):
+    assert dec8(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [
+    dict(bt=None), dict(sl=None), dict(bt=GOOD + 2), dict(sl=GOOD + 1),
+    dict(page=0), dict(page=4), dict(page=24), dict(page=1 << 17), dict(page=-16),
+    dict(num_pages=0), dict(max_pages=0),
+    dict(max_pages=7),                    # 7 * 16 < max_seq_len 128
+    dict(chunk=0), dict(chunk=8),         # chunk not a multiple of min(page, 128)
+    dict(page=256, chunk=64), dict(page=256, chunk=192),
+    dict(num_pages=1 << 30, page=1 << 16, max_pages=1),
+])
+def test_invalid_paged_decode_arguments(lib, kw):
+    assert decp(**kw) == fa.FA_ERR_INVALID_ARG
 
 
 def test_python_binding_raises_with_status(lib):
