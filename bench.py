@@ -4,7 +4,7 @@
 A step is one fa_fwd call (the whole prefill path: tile scheduling, TMA loads,
 S = QK^T, masking, online softmax, lazy O correction, P V, epilogue) over the
 headline workload, the causal MHA prefill B=2, H=16, N=M=2048, d=128, bf16;
-inputs are resident in HBM and L2 is flushed (a 256 MiB write) between steps.
+inputs are resident in HBM and L2 is flushed (a 256 MiB write, then a 256 MiB read, so that no dirty line is left to write back) between steps.
 Each step is timed with CUDA events on the launching stream.  The line also
 carries:
   roofline      the prefill kernel against the measured dense bf16 peak;
@@ -243,15 +243,40 @@ def bench_prefill(torch, fa, w, steps, warmup, flush, dist=None):
     return times
 
 
-def bench_decode(torch, fa, w, steps, warmup, flush, dist=None):
-    from exact_attention_05_gb300.workloads import workload_inputs
-    q, k, v = (t.cuda() for t in workload_inputs(w))
-    o = torch.empty_like(q)
+def decode_call(torch, fa, w, single_launch=False):
+    """Device-resident inputs of a decode workload and a zero-argument call of
+    the entry point that serves it: fa_decode (or fa_decode_fused with
+    ``single_launch``) for contiguous 16-bit K/V, fa_decode_fp8 for e4m3 K/V,
+    fa_decode_paged for a paged cache."""
+    from exact_attention_05_gb300.workloads import workload_decode_inputs
+    host = workload_decode_inputs(w)
+    if w.page > 0:
+        host.pop("k")
+        host.pop("v")
+    x = {name: t.cuda() for name, t in host.items()}
+    o = torch.empty_like(x["q"])
     lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    if w.kv == "e4m3":
+        if single_launch:
+            raise ValueError("the single launch is built for contiguous 16-bit K/V")
+        return lambda: fa.fa_decode_fp8(x["q"], x["k"], x["v"], x["k_scale"], x["v_scale"], o,
+                                        lse, w.B, w.Hq, w.Hkv, w.M, w.d, w.chunk, w.scale,
+                                        w.dtype)
+    if w.page > 0:
+        if single_launch:
+            raise ValueError("the single launch is built for contiguous 16-bit K/V")
+        bt = x["block_table"]
+        return lambda: fa.fa_decode_paged(x["q"], x["k_cache"], x["v_cache"], bt, x["seq_lens"],
+                                          o, lse, w.B, w.Hq, w.Hkv, w.M,
+                                          x["k_cache"].shape[0], w.page, bt.shape[1], w.d,
+                                          w.chunk, w.scale, w.dtype)
+    fn = fa.fa_decode_fused if single_launch else fa.fa_decode
+    return lambda: fn(x["q"], x["k"], x["v"], o, lse, w.B, w.Hq, w.Hkv, w.M, w.d, w.chunk,
+                      w.scale, w.dtype)
 
-    def call():
-        fa.fa_decode(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.M, w.d, w.chunk, w.scale, w.dtype)
 
+def bench_decode(torch, fa, w, steps, warmup, flush, dist=None, single_launch=False):
+    call = decode_call(torch, fa, w, single_launch)
     times = time_calls(torch, call, steps, warmup, flush, dist)
     if fa.fa_get_last_device_status() != fa.FA_OK:
         raise RuntimeError(f"{w.name}: a device-side wait expired")
@@ -259,19 +284,7 @@ def bench_decode(torch, fa, w, steps, warmup, flush, dist=None):
 
 
 def bench_decode_single_launch(torch, fa, w, steps, warmup, flush, dist=None):
-    from exact_attention_05_gb300.workloads import workload_inputs
-    q, k, v = (t.cuda() for t in workload_inputs(w))
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
-
-    def call():
-        fa.fa_decode_fused(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.M, w.d, w.chunk, w.scale,
-                           w.dtype)
-
-    times = time_calls(torch, call, steps, warmup, flush, dist)
-    if fa.fa_get_last_device_status() != fa.FA_OK:
-        raise RuntimeError(f"{w.name}: a device-side wait expired")
-    return times
+    return bench_decode(torch, fa, w, steps, warmup, flush, dist, single_launch=True)
 
 
 def bench_e2e_decode(torch, fa, w, steps, warmup):
@@ -413,6 +426,10 @@ def workload_config(w):
            "dtype": DTYPE_NAME[w.dtype], "causal": w.causal, "scale": w.scale}
     if w.kind == "decode":
         cfg["chunk"] = w.chunk
+        if w.kv != "16bit":
+            cfg["kv"] = w.kv
+        if w.page:
+            cfg["page"] = w.page
     if w.peaky_frac:
         cfg["peaky_k_rows"] = w.peaky_frac
     return cfg
@@ -428,7 +445,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE)
+    from exact_attention_05_gb300.workloads import WORKLOADS as _W
+    headline_ok = sorted(n for n, x in _W.items() if x.kv == "16bit" and x.page == 0)
+    ap.add_argument("--workload", default=HEADLINE, choices=headline_ok,
+                    help="the timed workload (the FP8 and paged decode workloads are timed "
+                         "in the per-workload table)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table, decode line and CPU baseline")
     args = ap.parse_args(argv)
@@ -453,11 +474,16 @@ def main(argv=None):
     peaks, peak_src = load_peaks()
     w = WORKLOADS[args.workload]
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_read = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
     flush_ctr = [0]
 
     def flush():
+        # write a buffer larger than L2, then read another one: L2 is left
+        # holding clean lines of neither input, so the timed call neither hits
+        # its inputs in L2 nor pays for writing back the flush's dirty lines
         flush_ctr[0] = (flush_ctr[0] + 1) & 0xFF
         flush_buf.fill_(flush_ctr[0])
+        flush_read.max()
 
     is_decode = w.kind == "decode"
     # work units of one step: FLOPs (prefill) or HBM bytes (decode), and their scale
@@ -514,12 +540,14 @@ def main(argv=None):
                     tt = bench_decode(torch, fa, wl, n, 3, fl, dist)
                     ms = max_over_ranks(statistics.median(tt), dist, device="cuda")
                     gbs = wl.decode_bytes / (ms * 1e-3) / 1e9
-                    ts = bench_decode_single_launch(torch, fa, wl, n, 3, fl, dist)
-                    ms1 = max_over_ranks(statistics.median(ts), dist, device="cuda")
-                    gbs1 = wl.decode_bytes / (ms1 * 1e-3) / 1e9
                     table[name] = {"ms": ms, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"],
-                                   "single_launch": {"ms": ms1, "GB/s": gbs1,
-                                                     "frac": gbs1 / peaks["hbm_gbs"]}}
+                                   "kv": wl.kv, "page": wl.page}
+                    if wl.kv != "e4m3" and wl.page == 0:
+                        ts = bench_decode_single_launch(torch, fa, wl, n, 3, fl, dist)
+                        ms1 = max_over_ranks(statistics.median(ts), dist, device="cuda")
+                        gbs1 = wl.decode_bytes / (ms1 * 1e-3) / 1e9
+                        table[name]["single_launch"] = {"ms": ms1, "GB/s": gbs1,
+                                                        "frac": gbs1 / peaks["hbm_gbs"]}
             extras["workloads"] = table
     clk = clocks.summary()
 
@@ -540,7 +568,7 @@ def main(argv=None):
                 "peak_source": f"{peak_src} HBM copy",
                 "note": "achieved over the whole call (chunk + merge kernels)"}
         l2 = "inputs larger than L2 (K/V vs 129 MB), no flush" if units >= 2 * L2_BYTES else \
-            "flushed between steps (256 MiB write)"
+            "flushed between steps (256 MiB write, then 256 MiB read)"
         launches = 2 * args.steps
     else:
         unit = "TFLOP/s"
@@ -548,7 +576,7 @@ def main(argv=None):
                 "unit": unit, "frac": achieved / peaks["bf16_tflops"],
                 "traffic": recorded_traffic(w.name, "prefill_kernel"),
                 "peak_source": f"{peak_src} dense bf16 burst"}
-        l2 = "flushed between steps (256 MiB write)"
+        l2 = "flushed between steps (256 MiB write, then 256 MiB read)"
         launches = args.steps
     line = {
         "metric": METRIC,

@@ -31,6 +31,7 @@
 //     seq_lens[b] keys (chunks past the end write an empty partial).
 #pragma once
 
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <cuda_fp8.h>
@@ -59,17 +60,35 @@ struct DecodeCfg {
     static constexpr int KBOX = ROW_BYTES < 128 ? ROW_BYTES : 128;  // swizzled K box row
     static constexpr int NSUBK = ROW_BYTES / KBOX;      // K boxes per row
     static constexpr int SUB_BYTES = TK * KBOX;         // one K sub-box
-    static constexpr int KQ = 256 / D;                  // key groups in the P.V step
-    static constexpr int TILE_BYTES = TK * ROW_BYTES;
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = TILE_BYTES;
-    static constexpr int QS_OFF = 2 * TILE_BYTES;                  // float [GMAX][D]
-    static constexpr int SC_OFF = QS_OFF + GMAX * D * 4;           // float [GMAX][TK]
-    static constexpr int RED_OFF = SC_OFF + GMAX * TK * 4;         // float2 [KQ-1][GMAX][D/2]
-    static constexpr int HS_OFF = RED_OFF + (KQ - 1) * GMAX * D * 4;  // per head m, l, alpha
-    static constexpr int BAR_OFF = HS_OFF + 3 * GMAX * 4;
-    static constexpr int MISC_OFF = BAR_OFF + 16;
-    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;        // + slack to align to 1 KB
+    static constexpr int TILE_BYTES = TK * ROW_BYTES;   // one K or one V sub-tile
+    static constexpr bool IS_F16 = DTypeFmt<T>::value == 0;
+    // Scores with a mixed-precision FMA (16-bit q times 16-bit k, fp32 sum)
+    // unless the keys are e4m3 and q is bf16 (e4m3 widens exactly to f16 only).
+    static constexpr bool QK_MIXED = !(FP8 && !IS_F16);
+    // P.V with the mixed FMA on f16 values (fp16 V, or e4m3 V widened to f16;
+    // P rounded to f16); bf16 V takes the fp32 route with fp32 P.
+    static constexpr bool PV_MIXED = FP8 || IS_F16;
+    static constexpr int QSZ = QK_MIXED ? 2 : 4;        // bytes per query element in smem
+    // P.V mapping: thread <-> (group of 4 columns, key group)
+    static constexpr int NCG = D / 4;
+    static constexpr int KQ = THREADS / NCG;            // key groups
+    static constexpr int KPG = TK / KQ;                 // keys per group
+    // Ring of tile slots that K and V sub-tiles stream through, in load order
+    // K0, V0, K1, V1, ...: 2 slots of 32 KB (16-bit, d = 128) up to 8 of 8 KB.
+    static constexpr int RING_BYTES = FP8 ? 32768 : 65536;
+    static constexpr int NSLOT = RING_BYTES / TILE_BYTES;
+    static constexpr int SC_OFF = RING_BYTES;                      // float [GMAX][TK]
+    static constexpr int PH_OFF = SC_OFF + GMAX * TK * 4;          // f16 P [GMAX][TK]
+    static constexpr int RED_OFF = PH_OFF + GMAX * TK * 2;         // float4 [KQ-1][GMAX][NCG]
+    static constexpr int HS_OFF = RED_OFF + (KQ - 1) * GMAX * D * 4;  // per warp max, sum [2][4][GMAX]
+    static constexpr int BAR_OFF = HS_OFF + 2 * 4 * GMAX * 4;      // NSLOT full barriers
+    static constexpr int MISC_OFF = BAR_OFF + 8 * NSLOT;
+    static constexpr int QS_OFF = MISC_OFF + 16;                   // q [g][D], sized at launch
+    static constexpr size_t smem_bytes(int g) {
+        return size_t(QS_OFF) + size_t(g) * D * QSZ + 1024;        // + slack to align to 1 KB
+    }
+    static_assert(NSLOT >= 2 && RING_BYTES % TILE_BYTES == 0, "ring of whole tiles");
+    static_assert(BAR_OFF % 8 == 0 && QS_OFF % 16 == 0, "alignment");
     // position of 16-byte chunk ch of K row i inside the swizzled box: the TMA
     // swizzle XORs the chunk index with address bits 7.. of the row start
     __device__ static int kchunk(int i, int ch) {
@@ -89,6 +108,32 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
     return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Mixed-precision FMAs (16-bit products, fp32 accumulators): c0 += a.lo * b.lo
+// and c1 += a.hi * b.hi for two packed pairs, or c0 += a.lo * p, c1 += a.hi * p.
+// The product of two 16-bit values is exact in fp32, so only the sum rounds.
+template <typename T>
+__device__ __forceinline__ void mfma2(float& c0, float& c1, uint32_t a, uint32_t b) {
+    if constexpr (DTypeFmt<T>::value == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+            "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+            : "+f"(c0), "+f"(c1) : "r"(a), "r"(b));
+    else
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t}"
+            : "+f"(c0), "+f"(c1) : "r"(a), "r"(b));
+}
+__device__ __forceinline__ void mfma2s_f16(float& c0, float& c1, uint32_t a, uint16_t p) {
+    asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, %3, %0;\n\tfma.rn.f32.f16 %1, a1, %3, %1;\n\t}"
+        : "+f"(c0), "+f"(c1) : "r"(a), "h"(p));
+}
+// Two e4m3 values (low byte first) -> f16x2 (exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
 }
 
 // Merges n partial results (fp32 rows of D at rows + i*D, normalised, with
@@ -260,11 +305,19 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
 
 // The chunk kernel.  FP8: K/V are e4m3 bytes with per-kv-head scales.  PAGED:
 // K/V come from a paged cache through a block table (see the file header).
-// GP query heads per pass over the tile (the host picks GP dividing the GQA
+// GP query heads per pass over a tile (the host picks GP dividing the GQA
 // group).  FUSED: the chunk kernel also merges (single launch); only for
 // contiguous 16-bit K/V.
+//
+// Persistent over chunks: the grid is (b, kv head) x nstripes; the CTA with
+// stripe s handles chunks s, s + nstripes, ... of its (b, kv head), so it loads
+// its g query rows (and, paged, its sequence length) once.  Warp 0 issues the
+// TMA copies of the K and V sub-tiles, in the order the chunks consume them,
+// into a ring of tile slots, and refills a slot as soon as the last pass over
+// it is done, so the next tiles stream in while the current one is computed.
+// Each chunk still yields its own partial (O_c, lse_c), as in Step 1.
 template <int D, typename T, bool FP8, bool PAGED, int GP, bool FUSED>
-__global__ void __launch_bounds__(128, 3)
+__global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const DecodeArgs a) {
     static_assert(!(FUSED && (FP8 || PAGED)), "the single launch is built for contiguous 16-bit K/V");
@@ -273,48 +326,30 @@ __global__ void __launch_bounds__(128, 3)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t kbar = sbase + C::BAR_OFF;
-    const uint32_t vbar = kbar + 8;
+    const uint32_t bar0 = sbase + C::BAR_OFF;  // full barrier of slot i at bar0 + 8 i
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
     float* qs = reinterpret_cast<float*>(smem + C::QS_OFF);
     float* sc = reinterpret_cast<float*>(smem + C::SC_OFF);
     float2* red = reinterpret_cast<float2*>(smem + C::RED_OFF);
-    float* hm = reinterpret_cast<float*>(smem + C::HS_OFF);
-    float* hl = hm + C::GMAX;
-    float* halpha = hl + C::GMAX;
-    const uint8_t* Ks = smem + C::K_OFF;
-    const uint8_t* Vs = smem + C::V_OFF;
+    float* wmax = reinterpret_cast<float*>(smem + C::HS_OFF);  // [warp][head] max of a sub-tile
+    float* wsum = wmax + 4 * C::GMAX;                             // [warp][head] sum of P
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    // Linear block index, (b, kv head) fastest: CTAs that run together read the
+    // Block index, (b, kv head) fastest: CTAs that run together read the
     // neighbouring heads of the same keys (whole contiguous key rows).
     const int nbh = a.B * a.Hkv;
-    const int c = blockIdx.x / nbh;
+    const int stripe = blockIdx.x / nbh;
     const int b = (blockIdx.x % nbh) / a.Hkv;
     const int kvh = blockIdx.x % a.Hkv;
     const int g = a.Hq / a.Hkv;
-    const int mb = PAGED ? min(__ldg(a.seq_lens + b), a.M) : a.M;  // keys of this batch
-    const int key0 = c * a.chunk;
-    const int key1 = min(mb, key0 + a.chunk);
+    const int npass = g / GP;
+    const int mb = PAGED ? min(__ldg(a.seq_lens + b), a.M) : a.M;  // keys of this sequence
     constexpr int NCP = D / 2;
 
-    if (key0 >= key1) {
-        // a chunk past the end of a shorter (paged) sequence: an empty partial,
-        // which the merge weighs with 2^-inf = 0
-        for (int gi = 0; gi < g; ++gi) {
-            const size_t pr = (size_t(b) * a.Hq + kvh * g + gi) * a.nc + c;
-            if (tid < NCP) reinterpret_cast<float2*>(a.o_part + pr * D)[tid] = make_float2(0.f, 0.f);
-            if (tid == 0) a.lse_part[pr] = -INFINITY;
-        }
-        return;
-    }
-    const int nsub = (key1 - key0 + C::TK - 1) / C::TK;
-
     if (tid == 0) {
-        mbar_init(kbar, 1);
-        mbar_init(vbar, 1);
+        for (int i = 0; i < C::NSLOT; ++i) mbar_init(bar0 + 8 * i, 1);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tensor_map(&tm_k);
@@ -323,225 +358,387 @@ __global__ void __launch_bounds__(128, 3)
     __syncthreads();
     const WaitCtl wc{abort_flag, a.status, a.timeout_ns};
 
-    int loads = 0;  // sub-tiles loaded so far (the phase of both barriers)
-    auto load_subtile = [&](int st) {
-        if (tid == 0) {
-            const int row = key0 + st * C::TK;
-            if constexpr (!PAGED) {
-                mbar_arrive_expect_tx(kbar, C::TILE_BYTES);
-#pragma unroll
-                for (int s = 0; s < C::NSUBK; ++s)
-                    tma_load_4d(sbase + C::K_OFF + s * C::SUB_BYTES, &tm_k, s * (C::KBOX / C::ESZ),
-                                kvh, row, b, kbar);
-                mbar_arrive_expect_tx(vbar, C::TILE_BYTES);
-                tma_load_4d(sbase + C::V_OFF, &tm_v, 0, kvh, row, b, vbar);
-            } else {
-                // one copy of R rows per page spanned; only the rows this chunk needs
+    // ---- producer (warp 0): walks this CTA's loads in consumption order -------
+    // Chunk c has nl loads: K, V of each sub-tile, once per pass if the chunk
+    // spans several sub-tiles, else once (the tile stays for all passes).
+    int p_c = stripe, p_li = 0, p_nl = 0, p_nsub = 1, p_key0 = 0, p_key1 = 0;
+    int issued = 0;
+    int pg_next = 0;  // paged: page id of this lane's copy of the next load
+    auto p_setup = [&]() {
+        // first chunk at or after p_c that has keys; p_c >= nc when none is left
+        for (; p_c < a.nc; p_c += a.nstripes) {
+            p_key0 = p_c * a.chunk;
+            p_key1 = min(mb, p_key0 + a.chunk);
+            if (p_key0 < p_key1) break;
+        }
+        if (p_c < a.nc) {
+            p_nsub = (p_key1 - p_key0 + C::TK - 1) / C::TK;
+            p_nl = 2 * (p_nsub > 1 ? p_nsub * npass : 1);
+            p_li = 0;
+        }
+    };
+    auto p_prefetch = [&]() {
+        if constexpr (PAGED) {
+            if (p_c < a.nc) {
                 const int R = a.page < C::TK ? a.page : C::TK;
-                const int nrows = min(C::TK, key1 - row);
-                const int ncopy = (nrows + R - 1) / R;
-                mbar_arrive_expect_tx(kbar, uint32_t(ncopy * R * C::ROW_BYTES));
-                mbar_arrive_expect_tx(vbar, uint32_t(ncopy * R * C::ROW_BYTES));
-                for (int r = 0; r < ncopy; ++r) {
-                    const int key = row + r * R;
-                    const int pg = __ldg(a.block_table + size_t(b) * a.max_pages + key / a.page);
-                    const int prow = key % a.page;
+                const int row = p_key0 + ((p_li >> 1) % p_nsub) * C::TK;
+                const int nrows = min(C::TK, p_key1 - row);
+                if (lane * R < nrows)
+                    pg_next = __ldg(a.block_table + size_t(b) * a.max_pages + (row + lane * R) / a.page);
+            }
+        }
+    };
+    auto p_issue = [&]() {
+        const int slot = issued % C::NSLOT;
+        const uint32_t bar = bar0 + 8 * slot;
+        const uint32_t dst = sbase + slot * C::TILE_BYTES;
+        const bool is_v = (p_li & 1) != 0;
+        const int row = p_key0 + ((p_li >> 1) % p_nsub) * C::TK;
+        if constexpr (!PAGED) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, C::TILE_BYTES);
+                if (!is_v) {
 #pragma unroll
                     for (int s = 0; s < C::NSUBK; ++s)
-                        tma_load_4d(sbase + C::K_OFF + s * C::SUB_BYTES + r * R * C::KBOX, &tm_k,
-                                    s * (C::KBOX / C::ESZ), kvh, prow, pg, kbar);
-                    tma_load_4d(sbase + C::V_OFF + r * R * C::ROW_BYTES, &tm_v, 0, kvh, prow, pg,
-                                vbar);
+                        tma_load_4d(dst + s * C::SUB_BYTES, &tm_k, s * (C::KBOX / C::ESZ), kvh, row,
+                                    b, bar);
+                } else {
+                    tma_load_4d(dst, &tm_v, 0, kvh, row, b, bar);
+                }
+            }
+        } else {
+            // one copy of R rows per page spanned (only the rows the chunk needs);
+            // lane r issues copy r
+            const int R = a.page < C::TK ? a.page : C::TK;
+            const int nrows = min(C::TK, p_key1 - row);
+            const int ncopy = (nrows + R - 1) / R;
+            if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(ncopy * R * C::ROW_BYTES));
+            __syncwarp();
+            if (lane < ncopy) {
+                const int prow = (row + lane * R) % a.page;
+                if (!is_v) {
+#pragma unroll
+                    for (int s = 0; s < C::NSUBK; ++s)
+                        tma_load_4d(dst + s * C::SUB_BYTES + lane * R * C::KBOX, &tm_k,
+                                    s * (C::KBOX / C::ESZ), kvh, prow, pg_next, bar);
+                } else {
+                    tma_load_4d(dst + lane * R * C::ROW_BYTES, &tm_v, 0, kvh, prow, pg_next, bar);
                 }
             }
         }
-        ++loads;
+        ++issued;
+        if (++p_li >= p_nl) {
+            p_c += a.nstripes;
+            p_setup();
+        }
+        p_prefetch();
     };
-    // The first sub-tile's copies go out before anything else.
-    load_subtile(0);
+    // keeps NSLOT loads ahead of the `released` loads the consumers are done with
+    auto produce = [&](int released) {
+        while (p_c < a.nc && issued < released + C::NSLOT) p_issue();
+    };
+    if (warp == 0) {
+        p_setup();
+        p_prefetch();
+        produce(0);
+    }
+
+    // query rows of all g heads of this kv head (read as broadcasts): the raw
+    // 16-bit values for the mixed-precision scores, else fp32
+    {
+        const T* qg = reinterpret_cast<const T*>(a.q) + (size_t(b) * a.Hq + kvh * g) * D;
+        for (int e = tid; e < g * D; e += C::THREADS) {
+            if constexpr (C::QK_MIXED)
+                reinterpret_cast<T*>(qs)[e] = qg[e];
+            else
+                qs[e] = static_cast<float>(qg[e]);
+        }
+    }
+    __syncthreads();
 
     const float kscale = FP8 ? __ldg(a.k_scale + kvh) : 1.f;
     const float vscale = FP8 ? __ldg(a.v_scale + kvh) : 1.f;
+    const float sfac = kscale * a.scale_log2;
     bool ok = true;
-    // P.V mapping: thread <-> (column pair cp, key group kq)
-    const int cp = tid % NCP;
-    const int kq = tid / NCP;
-    constexpr int KPG = C::TK / C::KQ;  // keys per group
-    for (int hg = 0; hg < g && ok; hg += GP) {
-        // this pass's query heads, as fp32 in shared memory (read as broadcasts)
-        for (int e = tid; e < GP * D; e += C::THREADS) {
-            const int gi = e / D, col = e % D;
-            const int h = kvh * g + hg + gi;
-            qs[e] = static_cast<float>(reinterpret_cast<const T*>(a.q)[(size_t(b) * a.Hq + h) * D + col]);
-        }
-        if (tid < C::GMAX) {
-            hm[tid] = -INFINITY;
-            hl[tid] = 0.f;
-        }
-        float2 acc[GP];
-#pragma unroll
-        for (int gi = 0; gi < GP; ++gi) acc[gi] = make_float2(0.f, 0.f);
+    int cn = 0;  // loads consumed (and released) so far
+    // P.V mapping: thread <-> (group of 4 columns cg, key group kq)
+    const int cg = tid % C::NCG;
+    const int kq = tid / C::NCG;
+    uint16_t* ph = reinterpret_cast<uint16_t*>(smem + C::PH_OFF);
 
-        for (int st = 0; st < nsub; ++st) {
-            const int ks = key0 + st * C::TK;
-            const int nk = min(C::TK, key1 - ks);
-            if (st > 0 || hg > 0) {
-                // a chunk of one sub-tile keeps its tile resident across head groups
-                if (nsub > 1) load_subtile(st);
+    for (int c = stripe; c < a.nc && ok; c += a.nstripes) {
+        const int key0 = c * a.chunk;
+        const int key1 = min(mb, key0 + a.chunk);
+        if (key0 >= key1) {
+            // a chunk past the end of a shorter (paged) sequence: an empty
+            // partial, which the merge weighs with 2^-inf = 0
+            for (int gi = 0; gi < g; ++gi) {
+                const size_t pr = (size_t(b) * a.Hq + kvh * g + gi) * a.nc + c;
+                if (tid < NCP) reinterpret_cast<float2*>(a.o_part + pr * D)[tid] = make_float2(0.f, 0.f);
+                if (tid == 0) a.lse_part[pr] = -INFINITY;
             }
-            const uint32_t ph = uint32_t(loads - 1) & 1u;
-            bool got = mbar_wait(kbar, ph, wc, FA_SITE_DECODE_KV);
-            if (!__syncthreads_and(got)) {
-                ok = false;
-                break;
+            continue;
+        }
+        const int nsub = (key1 - key0 + C::TK - 1) / C::TK;
+        for (int hg = 0; hg < g && ok; hg += GP) {
+            // the tile is given back after its last use: after every pass when the
+            // chunk spans several sub-tiles (each pass reloads them), else after the last
+            const bool release = nsub > 1 || hg + GP >= g;
+            // running max and sum of each head, kept (identically) by every thread
+            float m_run[GP], l_run[GP], alpha[GP];
+#pragma unroll
+            for (int gi = 0; gi < GP; ++gi) {
+                m_run[gi] = -INFINITY;
+                l_run[gi] = 0.f;
             }
-            // ---- scores: thread <-> key, full dot product from the swizzled K tile
-            {
-                constexpr int CH = C::KBOX / 16;  // 16-byte chunks per K box row
-                constexpr int EPC = 16 / C::ESZ;  // elements per chunk
-                const int i = tid;
-                float s[GP];
+            // two accumulators per head (even and odd keys): independent FMA chains
+            float4 acc[GP], acc2[GP];
 #pragma unroll
-                for (int gi = 0; gi < GP; ++gi) s[gi] = 0.f;
+            for (int gi = 0; gi < GP; ++gi) acc[gi] = acc2[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+            for (int st = 0; st < nsub; ++st) {
+                const int nk = min(C::TK, key1 - (key0 + st * C::TK));
+                const int kslot = cn % C::NSLOT;
+                const int vslot = (cn + 1) % C::NSLOT;
+                const uint8_t* Ks = smem + kslot * C::TILE_BYTES;
+                const uint8_t* Vs = smem + vslot * C::TILE_BYTES;
+                bool got = mbar_wait(bar0 + 8 * kslot, uint32_t(cn / C::NSLOT) & 1u, wc,
+                                     FA_SITE_DECODE_KV);
+                if (!__syncthreads_and(got)) {
+                    ok = false;
+                    break;
+                }
+                // ---- scores: thread <-> key, full dot product from the swizzled K tile,
+                // four partial sums per head (independent FMA chains); then the
+                // max of each warp's 32 keys
+                float tsc[GP];
+                {
+                    constexpr int CH = C::KBOX / 16;  // 16-byte chunks per K box row
+                    constexpr int EPC = 16 / C::ESZ;  // elements per chunk
+                    const int i = tid;
+                    float s[GP][4];
 #pragma unroll
-                for (int sub = 0; sub < C::NSUBK; ++sub) {
+                    for (int gi = 0; gi < GP; ++gi) s[gi][0] = s[gi][1] = s[gi][2] = s[gi][3] = 0.f;
 #pragma unroll
-                    for (int ch = 0; ch < CH; ++ch) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(
-                            Ks + sub * C::SUB_BYTES + i * C::KBOX + (C::kchunk(i, ch) << 4));
-                        float kf[EPC];
-                        if constexpr (FP8) {
-                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                    for (int sub = 0; sub < C::NSUBK; ++sub) {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const float2 lo = e4m3x2_to_float2(uint16_t(ww[u] & 0xffffu));
-                                const float2 hi = e4m3x2_to_float2(uint16_t(ww[u] >> 16));
-                                kf[4 * u] = lo.x;
-                                kf[4 * u + 1] = lo.y;
-                                kf[4 * u + 2] = hi.x;
-                                kf[4 * u + 3] = hi.y;
+                        for (int ch = 0; ch < CH; ++ch) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(
+                                Ks + sub * C::SUB_BYTES + i * C::KBOX + (C::kchunk(i, ch) << 4));
+                            const int col = sub * (C::KBOX / C::ESZ) + ch * EPC;
+                            if constexpr (C::QK_MIXED) {
+                                // k as packed 16-bit pairs: kw[m] holds elements 2m, 2m+1
+                                constexpr int NW = EPC / 2;
+                                uint32_t kw[NW];
+                                if constexpr (FP8) {
+                                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u) {
+                                        kw[2 * u] = e4m3x2_to_f16x2(uint16_t(ww[u] & 0xffffu));
+                                        kw[2 * u + 1] = e4m3x2_to_f16x2(uint16_t(ww[u] >> 16));
+                                    }
+                                } else {
+                                    kw[0] = w.x;
+                                    kw[1] = w.y;
+                                    kw[2] = w.z;
+                                    kw[3] = w.w;
+                                }
+                                const T* qb = reinterpret_cast<const T*>(qs) + (hg) * D + col;
+#pragma unroll
+                                for (int gi = 0; gi < GP; ++gi) {
+#pragma unroll
+                                    for (int m4 = 0; m4 < NW; m4 += 4) {
+                                        const uint4 qw =
+                                            *reinterpret_cast<const uint4*>(qb + gi * D + 2 * m4);
+                                        mfma2<T>(s[gi][0], s[gi][1], kw[m4], qw.x);
+                                        mfma2<T>(s[gi][2], s[gi][3], kw[m4 + 1], qw.y);
+                                        mfma2<T>(s[gi][0], s[gi][1], kw[m4 + 2], qw.z);
+                                        mfma2<T>(s[gi][2], s[gi][3], kw[m4 + 3], qw.w);
+                                    }
+                                }
+                            } else {
+                                float kf[EPC];
+                                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const float2 lo = e4m3x2_to_float2(uint16_t(ww[u] & 0xffffu));
+                                    const float2 hi = e4m3x2_to_float2(uint16_t(ww[u] >> 16));
+                                    kf[4 * u] = lo.x;
+                                    kf[4 * u + 1] = lo.y;
+                                    kf[4 * u + 2] = hi.x;
+                                    kf[4 * u + 3] = hi.y;
+                                }
+                                const float* qb = qs + hg * D + col;
+#pragma unroll
+                                for (int gi = 0; gi < GP; ++gi) {
+#pragma unroll
+                                    for (int e4 = 0; e4 < EPC; e4 += 4) {
+                                        const float4 qv =
+                                            *reinterpret_cast<const float4*>(qb + gi * D + e4);
+                                        s[gi][0] = fmaf(qv.x, kf[e4], s[gi][0]);
+                                        s[gi][1] = fmaf(qv.y, kf[e4 + 1], s[gi][1]);
+                                        s[gi][2] = fmaf(qv.z, kf[e4 + 2], s[gi][2]);
+                                        s[gi][3] = fmaf(qv.w, kf[e4 + 3], s[gi][3]);
+                                    }
+                                }
                             }
-                        } else {
-                            unpack8<T>(w, kf);
-                        }
-                        const int col = sub * (C::KBOX / C::ESZ) + ch * EPC;
-#pragma unroll
-                        for (int gi = 0; gi < GP; ++gi) {
-                            float t = s[gi];
-#pragma unroll
-                            for (int e4 = 0; e4 < EPC; e4 += 4) {
-                                const float4 qv = *reinterpret_cast<const float4*>(qs + gi * D + col + e4);
-                                t = fmaf(qv.x, kf[e4], t);
-                                t = fmaf(qv.y, kf[e4 + 1], t);
-                                t = fmaf(qv.z, kf[e4 + 2], t);
-                                t = fmaf(qv.w, kf[e4 + 3], t);
-                            }
-                            s[gi] = t;
                         }
                     }
+#pragma unroll
+                    for (int gi = 0; gi < GP; ++gi) {
+                        const float t = (s[gi][0] + s[gi][1]) + (s[gi][2] + s[gi][3]);
+                        tsc[gi] = i < nk ? t * sfac : -INFINITY;
+                        float mx = tsc[gi];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                        if (lane == 0) wmax[warp * C::GMAX + gi] = mx;
+                    }
                 }
-                const float sfac = kscale * a.scale_log2;
-#pragma unroll
-                for (int gi = 0; gi < GP; ++gi) sc[gi * C::TK + i] = i < nk ? s[gi] * sfac : -INFINITY;
-            }
-            __syncthreads();
-            // ---- softmax update of each head (one warp per head)
-            for (int gi = warp; gi < GP; gi += 4) {
-                float* srow = sc + gi * C::TK;
-                float v[C::TK / 32];
-                float mx = -INFINITY;
-#pragma unroll
-                for (int t = 0; t < C::TK / 32; ++t) {
-                    v[t] = srow[lane + 32 * t];
-                    mx = fmaxf(mx, v[t]);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float m_old = hm[gi];
-                const float m_new = fmaxf(m_old, mx);
-                const float alpha = fast_exp2(m_old - m_new);  // 0 on the first sub-tile
-                float sum = 0.f;
-#pragma unroll
-                for (int t = 0; t < C::TK / 32; ++t) {
-                    const float p = fast_exp2(v[t] - m_new);  // masked keys give exp2(-inf) = 0
-                    srow[lane + 32 * t] = p;
-                    sum += p;
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                if (lane == 0) {
-                    hm[gi] = m_new;
-                    hl[gi] = hl[gi] * alpha + sum;
-                    halpha[gi] = alpha;
-                }
-            }
-            got = mbar_wait(vbar, ph, wc, FA_SITE_DECODE_KV);
-            if (!__syncthreads_and(got)) {
-                ok = false;
-                break;
-            }
-            // ---- O_acc = alpha * O_acc + P V over this thread's key group and column pair
-#pragma unroll
-            for (int gi = 0; gi < GP; ++gi) {
-                const float al = halpha[gi];
-                acc[gi].x *= al;
-                acc[gi].y *= al;
-            }
-            const int j0 = kq * KPG;
-            const int j1 = min(j0 + KPG, nk);
-#pragma unroll 4
-            for (int j = j0; j < j1; ++j) {
-                float2 vf;
-                if constexpr (FP8)
-                    vf = e4m3x2_to_float2(reinterpret_cast<const uint16_t*>(Vs)[j * NCP + cp]);
-                else
-                    vf = unpack2<T>(reinterpret_cast<const uint32_t*>(Vs)[j * NCP + cp]);
+                __syncthreads();
+                // the K tile is consumed: refill its slot
+                if (release && warp == 0) produce(cn + 1);
+                // ---- softmax update: thread <-> key for every head (P of its own
+                // score), the sub-tile max from the four warp maxima
 #pragma unroll
                 for (int gi = 0; gi < GP; ++gi) {
-                    const float p = sc[gi * C::TK + j];
-                    acc[gi].x = fmaf(p, vf.x, acc[gi].x);
-                    acc[gi].y = fmaf(p, vf.y, acc[gi].y);
+                    const float mx = fmaxf(fmaxf(wmax[gi], wmax[C::GMAX + gi]),
+                                           fmaxf(wmax[2 * C::GMAX + gi], wmax[3 * C::GMAX + gi]));
+                    const float m_new = fmaxf(m_run[gi], mx);
+                    alpha[gi] = fast_exp2(m_run[gi] - m_new);  // 0 on the first sub-tile
+                    m_run[gi] = m_new;
+                    float p = fast_exp2(tsc[gi] - m_new);  // masked keys give exp2(-inf) = 0
+                    if constexpr (C::PV_MIXED) {
+                        // P.V takes P in f16; l sums the same rounded values
+                        const __half hp = __float2half_rn(p);
+                        ph[gi * C::TK + tid] = __half_as_ushort(hp);
+                        p = __half2float(hp);
+                    } else {
+                        sc[gi * C::TK + tid] = p;
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+                    if (lane == 0) wsum[warp * C::GMAX + gi] = p;
+                }
+                got = mbar_wait(bar0 + 8 * vslot, uint32_t((cn + 1) / C::NSLOT) & 1u, wc,
+                                FA_SITE_DECODE_KV);
+                if (!__syncthreads_and(got)) {
+                    ok = false;
+                    break;
+                }
+                // ---- O_acc = alpha * O_acc + P V over this thread's key group and 4 columns
+#pragma unroll
+                for (int gi = 0; gi < GP; ++gi) {
+                    const float al = alpha[gi];
+                    l_run[gi] = l_run[gi] * al + ((wsum[gi] + wsum[C::GMAX + gi]) +
+                                                  (wsum[2 * C::GMAX + gi] + wsum[3 * C::GMAX + gi]));
+                    acc[gi].x *= al;
+                    acc[gi].y *= al;
+                    acc[gi].z *= al;
+                    acc[gi].w *= al;
+                    acc2[gi].x *= al;
+                    acc2[gi].y *= al;
+                    acc2[gi].z *= al;
+                    acc2[gi].w *= al;
+                }
+                // columns 4cg .. 4cg+3 of V row j as two packed pairs (f16 on the mixed route)
+                auto vquad = [&](int j) {
+                    uint2 r;
+                    if constexpr (FP8) {
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + j * C::ROW_BYTES + cg * 4);
+                        r.x = e4m3x2_to_f16x2(uint16_t(w & 0xffffu));
+                        r.y = e4m3x2_to_f16x2(uint16_t(w >> 16));
+                    } else {
+                        r = *reinterpret_cast<const uint2*>(Vs + j * C::ROW_BYTES + cg * 8);
+                    }
+                    return r;
+                };
+                auto pv = [&](float4& o, uint2 vq, int gi, int j) {
+                    if constexpr (C::PV_MIXED) {
+                        const uint16_t pj = ph[gi * C::TK + j];
+                        mfma2s_f16(o.x, o.y, vq.x, pj);
+                        mfma2s_f16(o.z, o.w, vq.y, pj);
+                    } else {
+                        const float pj = sc[gi * C::TK + j];
+                        const float2 a0 = unpack2<T>(vq.x), a1 = unpack2<T>(vq.y);
+                        o.x = fmaf(pj, a0.x, o.x);
+                        o.y = fmaf(pj, a0.y, o.y);
+                        o.z = fmaf(pj, a1.x, o.z);
+                        o.w = fmaf(pj, a1.y, o.w);
+                    }
+                };
+                const int j0 = kq * C::KPG;
+                const int j1 = min(j0 + C::KPG, nk);
+                int j = j0;
+#pragma unroll 2
+                for (; j + 1 < j1; j += 2) {
+                    const uint2 v0 = vquad(j), v1 = vquad(j + 1);
+#pragma unroll
+                    for (int gi = 0; gi < GP; ++gi) {
+                        pv(acc[gi], v0, gi, j);
+                        pv(acc2[gi], v1, gi, j + 1);
+                    }
+                }
+                if (j < j1) {
+                    const uint2 v0 = vquad(j);
+#pragma unroll
+                    for (int gi = 0; gi < GP; ++gi) pv(acc[gi], v0, gi, j);
+                }
+                __syncthreads();  // the V tile and the scores may be overwritten next
+                if (release) {
+                    if (warp == 0) produce(cn + 2);
+                    cn += 2;
                 }
             }
-            __syncthreads();  // the tile and the scores may be overwritten next
-        }
-        if (!ok) break;
-        // ---- combine the key groups and write the chunk partials (fp32, log2-domain lse)
-        if (kq > 0) {
-#pragma unroll
-            for (int gi = 0; gi < GP; ++gi) red[((kq - 1) * C::GMAX + gi) * NCP + cp] = acc[gi];
-        }
-        __syncthreads();
-        if (kq == 0) {
+            if (!ok) break;
+            // ---- combine the key groups and write the chunk partials (fp32, log2-domain lse)
+            float4* red4 = reinterpret_cast<float4*>(red);
 #pragma unroll
             for (int gi = 0; gi < GP; ++gi) {
-                float2 t = acc[gi];
-#pragma unroll
-                for (int u = 1; u < C::KQ; ++u) {
-                    const float2 o = red[((u - 1) * C::GMAX + gi) * NCP + cp];
-                    t.x += o.x;
-                    t.y += o.y;
-                }
-                const int h = kvh * g + hg + gi;
-                const size_t pr = (size_t(b) * a.Hq + h) * a.nc + c;
-                const float inv = vscale / hl[gi];
-                reinterpret_cast<float2*>(a.o_part + pr * D)[cp] = make_float2(t.x * inv, t.y * inv);
-                if (cp == 0) a.lse_part[pr] = hm[gi] + log2f(hl[gi]);
+                acc[gi].x += acc2[gi].x;
+                acc[gi].y += acc2[gi].y;
+                acc[gi].z += acc2[gi].z;
+                acc[gi].w += acc2[gi].w;
             }
+            if (kq > 0) {
+#pragma unroll
+                for (int gi = 0; gi < GP; ++gi) red4[((kq - 1) * C::GMAX + gi) * C::NCG + cg] = acc[gi];
+            }
+            __syncthreads();
+            if (kq == 0) {
+#pragma unroll
+                for (int gi = 0; gi < GP; ++gi) {
+                    float4 t = acc[gi];
+#pragma unroll
+                    for (int u = 1; u < C::KQ; ++u) {
+                        const float4 o = red4[((u - 1) * C::GMAX + gi) * C::NCG + cg];
+                        t.x += o.x;
+                        t.y += o.y;
+                        t.z += o.z;
+                        t.w += o.w;
+                    }
+                    const int h = kvh * g + hg + gi;
+                    const size_t pr = (size_t(b) * a.Hq + h) * a.nc + c;
+                    const float inv = vscale / l_run[gi];
+                    reinterpret_cast<float4*>(a.o_part + pr * D)[cg] =
+                        make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+                    if (cg == 0) a.lse_part[pr] = m_run[gi] + log2f(l_run[gi]);
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
+        if constexpr (FUSED) fused_merge_tail<D, T>(a, ok, b, kvh, c);
     }
-    // every issued copy must have landed before the CTA exits
-    if (tid == 0 && loads > 0) {
-        mbar_drain_wait(kbar, uint32_t(loads - 1) & 1u, wc, FA_SITE_DRAIN);
-        mbar_drain_wait(vbar, uint32_t(loads - 1) & 1u, wc, FA_SITE_DRAIN);
+    // every issued copy must have landed before the CTA exits (only a wait that
+    // gave up leaves any outstanding)
+    if (tid == 0) {
+        for (int n = max(cn, issued - C::NSLOT); n < issued; ++n)
+            mbar_drain_wait(bar0 + 8 * (n % C::NSLOT), uint32_t(n / C::NSLOT) & 1u, wc,
+                            FA_SITE_DRAIN);
     }
     if constexpr (!FUSED) {
         // this CTA's partials are written: the merge grid may be scheduled
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    } else {
-        fused_merge_tail<D, T>(a, ok, b, kvh, c);
     }
 }
 
@@ -581,12 +778,44 @@ cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
                          cudaStream_t stream) {
     using C = DecodeCfg<D, T, FP8>;
     auto kern = chunk_kernel<D, T, FP8, PAGED, GP, FUSED>;
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    const int g = a.Hq / a.Hkv;
+    const size_t smem = C::smem_bytes(g);
+    if (smem > size_t(227) * 1024) return cudaErrorInvalidConfiguration;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(smem));
     if (err != cudaSuccess) return err;
-    const long long nblocks = (long long)a.nc * a.B * a.Hkv;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               int(cudaSharedmemCarveoutMaxShared));
+    if (err != cudaSuccess) return err;
+    // resident CTAs per SM for this shared-memory size (cached: it depends on g only)
+    static std::atomic<long long> cached{-1};
+    long long cv = cached.load(std::memory_order_relaxed);
+    int occ = 0;
+    if (cv >= 0 && (cv >> 8) == (long long)smem) {
+        occ = int(cv & 0xff);
+    } else {
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, smem);
+        if (err != cudaSuccess) return err;
+        occ = occ < 1 ? 1 : (occ > 255 ? 255 : occ);
+        cached.store(((long long)smem << 8) | occ, std::memory_order_relaxed);
+    }
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return err;
+    // one wave of persistent CTAs: every (b, kv head) gets the same number of
+    // stripes, as many as fit (at least one)
+    const long long nbh = (long long)a.B * a.Hkv;
+    long long nstripes = (long long)occ * sms / nbh;
+    nstripes = nstripes < 1 ? 1 : (nstripes > a.nc ? a.nc : nstripes);
+    // the single launch keeps one chunk per CTA: a CTA that merges a group must
+    // not hold up a stream of further chunks behind it
+    if (FUSED) nstripes = a.nc;
+    const long long nblocks = nbh * nstripes;
     if (nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<dim3((unsigned)nblocks), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(tk, tv, a);
+    DecodeArgs la = a;
+    la.nstripes = int(nstripes);
+    kern<<<dim3((unsigned)nblocks), dim3(C::THREADS), smem, stream>>>(tk, tv, la);
     return cudaGetLastError();
 }
 

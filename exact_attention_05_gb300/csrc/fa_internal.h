@@ -42,6 +42,7 @@ struct DecodeArgs {
     float* o_part;         // workspace [B, Hq, nc, d] fp32
     float* lse_part;       // workspace [B, Hq, nc] fp32, log2 domain
     int B, Hq, Hkv, M, chunk, nc;
+    int nstripes;          // CTAs per (b, kv head); set by the launcher
     float scale_log2;
     int* status;
     unsigned long long timeout_ns;
