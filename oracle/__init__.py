@@ -79,6 +79,9 @@ def _load():
         lib.oracle_decode_chunked.argtypes = [u16p, u16p, u16p, I, I, I, I, I, I, I, D,
                                               f64p, f64p, f64p, f64p]
         lib.oracle_decode_chunked.restype = I
+        lib.oracle_attention_backward.argtypes = [u16p, u16p, u16p, u16p, I, I, I, I, I, I, I,
+                                                  I, D, f64p, f64p, f64p]
+        lib.oracle_attention_backward.restype = I
         u8p = ctypes.POINTER(ctypes.c_uint8)
         f32p = ctypes.POINTER(ctypes.c_float)
         i32p = ctypes.POINTER(ctypes.c_int32)
@@ -197,6 +200,29 @@ def decode_chunked(q, k, v, dtype, chunk, scale):
     if rc != 0:
         raise ValueError("oracle_decode_chunked rejected its arguments")
     return op, lp, o, lse
+
+
+def attention_backward(q, k, v, dout, dtype, causal, scale):
+    """Gradients of exact attention: q, dout [B,N,Hq,d], k/v [B,M,Hkv,d] (uint16
+    bit arrays).  Returns (dQ [B,N,Hq,d], dK [B,M,Hkv,d], dV [B,M,Hkv,d]) fp64."""
+    lib = _load()
+    B, N, Hq, d = q.shape
+    _, M, Hkv, _ = k.shape
+    if dout.shape != q.shape or k.shape != v.shape:
+        raise ValueError("shape mismatch")
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    dout, dp = _u16(dout)
+    dq = np.zeros((B, N, Hq, d), np.float64)
+    dk = np.zeros((B, M, Hkv, d), np.float64)
+    dv = np.zeros((B, M, Hkv, d), np.float64)
+    rc = lib.oracle_attention_backward(qp, kp, vp, dp, int(dtype), B, Hq, Hkv, N, M, d,
+                                       int(bool(causal)), float(scale), _f64(dq), _f64(dk),
+                                       _f64(dv))
+    if rc != 0:
+        raise ValueError("oracle_attention_backward rejected its arguments")
+    return dq, dk, dv
 
 
 def e4m3(bits: np.ndarray) -> np.ndarray:

@@ -33,6 +33,10 @@
  *   log sum_c exp(lse_c - m), w_c = exp(lse_c - global_lse), O = sum_c w_c
  *   O_c).
  *
+ *   backward, "Tensor Core 迁移计划" (phase 2: the backward's contractions
+ *   dV = P^T dO, dP = dO V^T, dQ and dK from dS): the gradients of O with
+ *   respect to Q, K and V by the chain rule through the softmax.
+ *
  *   FP8 K/V decode: attention over K = k_scale[h] * e4m3(k8), V likewise,
  *   with the OCP E4M3 format decoded from its definition.
  *
@@ -318,6 +322,109 @@ int oracle_decode_chunked(const uint16_t* q, const uint16_t* k, const uint16_t* 
         free(prow);
         free(Oc);
         free(Lc);
+    }
+    return failed ? -1 : 0;
+}
+
+/* ---- backward: gradients of O with respect to Q, K and V ------------------ */
+
+/*
+ * The gradients of the attention above, for an upstream gradient dO [B,N,Hq,d]
+ * (the training step after the forward; "Tensor Core 迁移计划", phase 2, names
+ * the backward's contractions dV = P^T dO, dP = dO V^T and dQ, dK from dS).
+ * With s_ij = scale q_i . k_j over the visible keys and p_ij its softmax, the
+ * chain rule through o_i = sum_j p_ij v_j and the softmax Jacobian gives
+ *     dV_j  = sum_i p_ij dO_i,
+ *     dP_ij = dO_i . v_j,
+ *     dS_ij = p_ij (dP_ij - sum_k p_ik dP_ik),
+ *     dQ_i  = scale sum_j dS_ij k_j,
+ *     dK_j  = scale sum_i dS_ij q_i,
+ * with dK and dV of kv head kh summed over the g query heads that read it.
+ * Every P row, dP row and dS row is formed explicitly (no D_i = dO_i . O_i
+ * shortcut, no online rescaling).  dq [B,N,Hq,d], dk/dv [B,M,Hkv,d], fp64.
+ * Returns 0, or -1 on a bad shape or an allocation failure.
+ */
+int oracle_attention_backward(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                              const uint16_t* dout, int dtype, int B, int Hq, int Hkv, int N,
+                              int M, int d, int causal, double scale, double* dq, double* dk,
+                              double* dv) {
+    if (check_shape(B, Hq, Hkv, N, M, d)) return -1;
+    const int g = Hq / Hkv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int task = 0; task < B * Hkv; ++task) {
+        const int b = task / Hkv, kh = task % Hkv;
+        double* K = malloc(sizeof(double) * (size_t)M * d);
+        double* V = malloc(sizeof(double) * (size_t)M * d);
+        double* dK = calloc((size_t)M * d, sizeof(double));
+        double* dV = calloc((size_t)M * d, sizeof(double));
+        double* qrow = malloc(sizeof(double) * (size_t)d);
+        double* dorow = malloc(sizeof(double) * (size_t)d);
+        double* P = malloc(sizeof(double) * (size_t)M);
+        double* dP = malloc(sizeof(double) * (size_t)M);
+        double* dS = malloc(sizeof(double) * (size_t)M);
+        if (!K || !V || !dK || !dV || !qrow || !dorow || !P || !dP || !dS) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+            gather_head(k, dtype, b, kh, M, Hkv, d, K);
+            gather_head(v, dtype, b, kh, M, Hkv, d, V);
+            for (int h = kh * g; h < (kh + 1) * g; ++h) {
+                for (int i = 0; i < N; ++i) {
+                    const size_t row = (((size_t)b * N + i) * Hq + h) * (size_t)d;
+                    decode_array(q + row, qrow, (size_t)d, dtype);
+                    decode_array(dout + row, dorow, (size_t)d, dtype);
+                    const int nk = keys_visible(i, M, causal);
+                    /* P row: softmax of s_ij = scale q_i . k_j */
+                    double m = -INFINITY;
+                    for (int j = 0; j < nk; ++j) {
+                        double acc = 0.0;
+                        for (int t = 0; t < d; ++t) acc += qrow[t] * K[(size_t)j * d + t];
+                        P[j] = scale * acc;
+                        if (P[j] > m) m = P[j];
+                    }
+                    double l = 0.0;
+                    for (int j = 0; j < nk; ++j) {
+                        P[j] = exp(P[j] - m);
+                        l += P[j];
+                    }
+                    for (int j = 0; j < nk; ++j) P[j] /= l;
+                    /* dP row and the softmax Jacobian */
+                    double pdp = 0.0;
+                    for (int j = 0; j < nk; ++j) {
+                        double acc = 0.0;
+                        for (int t = 0; t < d; ++t) acc += dorow[t] * V[(size_t)j * d + t];
+                        dP[j] = acc;
+                        pdp += P[j] * dP[j];
+                    }
+                    for (int j = 0; j < nk; ++j) dS[j] = P[j] * (dP[j] - pdp);
+                    /* dQ_i, and this row's terms of dK and dV */
+                    double* dqrow = dq + row;
+                    for (int t = 0; t < d; ++t) dqrow[t] = 0.0;
+                    for (int j = 0; j < nk; ++j) {
+                        for (int t = 0; t < d; ++t) {
+                            dqrow[t] += scale * dS[j] * K[(size_t)j * d + t];
+                            dK[(size_t)j * d + t] += scale * dS[j] * qrow[t];
+                            dV[(size_t)j * d + t] += P[j] * dorow[t];
+                        }
+                    }
+                }
+            }
+            for (int j = 0; j < M; ++j) {
+                const size_t dst = (((size_t)b * M + j) * Hkv + kh) * (size_t)d;
+                memcpy(dk + dst, dK + (size_t)j * d, sizeof(double) * (size_t)d);
+                memcpy(dv + dst, dV + (size_t)j * d, sizeof(double) * (size_t)d);
+            }
+        }
+        free(K);
+        free(V);
+        free(dK);
+        free(dV);
+        free(qrow);
+        free(dorow);
+        free(P);
+        free(dP);
+        free(dS);
     }
     return failed ? -1 : 0;
 }
