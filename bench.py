@@ -243,6 +243,28 @@ def bench_prefill(torch, fa, w, steps, warmup, flush, dist=None):
     return times
 
 
+def bench_backward(torch, fa, w, steps, warmup, flush, dist=None):
+    """fa_bwd on a prefill workload: O and LSE come from one untimed fa_fwd; dO is
+    iid N(0, 1) in the workload's type.  Algorithmic FLOPs: 2.5x the forward's
+    (five GEMMs of 2*N*M*d per head instead of two)."""
+    from exact_attention_05_gb300.workloads import make_dout, workload_inputs
+    q, k, v = (t.cuda() for t in workload_inputs(w))
+    dout = make_dout(w.B, w.N, w.Hq, w.d, w.dtype, w.seed + 7).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.M, w.d, int(w.causal), w.scale, w.dtype)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def call():
+        fa.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, w.B, w.Hq, w.Hkv, w.N, w.M, w.d,
+                  int(w.causal), w.scale, w.dtype)
+
+    times = time_calls(torch, call, steps, warmup, flush, dist)
+    if fa.fa_get_last_device_status() != fa.FA_OK:
+        raise RuntimeError(f"{w.name}: a device-side wait expired (backward)")
+    return times
+
+
 def decode_call(torch, fa, w, single_launch=False):
     """Device-resident inputs of a decode workload and a zero-argument call of
     the entry point that serves it: fa_decode (or fa_decode_fused with
@@ -535,6 +557,13 @@ def main(argv=None):
                     ms = max_over_ranks(statistics.median(tt), dist, device="cuda")
                     tf = wl.flops / (ms * 1e-3) / 1e12
                     table[name] = {"ms": ms, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]}
+                    tb = bench_backward(torch, fa, wl, n, 3, flush if wl.flops < 1e12 else None,
+                                        dist)
+                    msb = max_over_ranks(statistics.median(tb), dist, device="cuda")
+                    tfb = 2.5 * wl.flops / (msb * 1e-3) / 1e12
+                    table[name]["backward"] = {"ms": msb, "TFLOP/s": tfb,
+                                               "frac": tfb / peaks["bf16_tflops"],
+                                               "launches_per_call": 3}
                 else:
                     fl = flush if wl.decode_bytes < 2 * L2_BYTES else None
                     tt = bench_decode(torch, fa, wl, n, 3, fl, dist)

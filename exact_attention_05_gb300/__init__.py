@@ -64,6 +64,8 @@ def load_library():
         I, F = ctypes.c_int, ctypes.c_float
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, I, F, I, vp]
         lib.fa_fwd.restype = I
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, I, I, I, I, I, I, I, F, I, vp]
+        lib.fa_bwd.restype = I
         lib.fa_decode.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
         lib.fa_decode.restype = I
         lib.fa_decode_fused.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
@@ -124,6 +126,17 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, M, d, causal, scale, dtype, stream=No
                                int(Hkv), int(N), int(M), int(d), int(causal), float(scale),
                                int(dtype), _stream(stream))
     return _check(st, "fa_fwd") if check else st
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, M, d, causal, scale, dtype,
+           stream=None, check=True) -> int:
+    """Backward of fa_fwd: dq [B,N,Hq,d], dk/dv [B,M,Hkv,d] from dout and the
+    forward's o and lse."""
+    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                               _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(N),
+                               int(M), int(d), int(causal), float(scale), int(dtype),
+                               _stream(stream))
+    return _check(st, "fa_bwd") if check else st
 
 
 def fa_decode(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, dtype, stream=None,
@@ -291,3 +304,21 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, c
                     num_pages, page_size, block_table.shape[1], d, chunk, scale, _dtype_code(q),
                     stream)
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None,
+                       dv=None, stream=None):
+    """dQ, dK, dV of attention_forward(q, k, v, causal, scale) -> (o, lse) for the
+    upstream gradient dout [B,N,Hq,d]; all contiguous CUDA tensors."""
+    import torch
+    B, N, Hq, d = q.shape
+    _, M, Hkv, _ = k.shape
+    for t in (q, k, v, o, lse, dout):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, M, d, int(bool(causal)), scale,
+           _dtype_code(q), stream)
+    return dq, dk, dv

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu", "fa_decode_fp8.cu", "fa_decode_paged.cu",
+SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_backward.cu", "fa_decode.cu", "fa_decode_fp8.cu", "fa_decode_paged.cu",
            "fa_decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

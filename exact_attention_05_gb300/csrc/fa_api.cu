@@ -228,6 +228,54 @@ FA_EXPORT fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
     return from_cuda(fa::launch_prefill(tq, tk, tv, to, a, d, (int)dtype, (cudaStream_t)stream));
 }
 
+FA_EXPORT fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                           int Hq, int Hkv, int N, int M, int d, int causal, float scale,
+                           fa_dtype dtype, fa_stream_t stream) {
+    fa_status s = check_args(q, k, v, o, lse, B, Hq, Hkv, N, M, d, scale, (int)dtype);
+    if (s != FA_OK) return s;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+        return FA_ERR_INVALID_ARG;
+    const long long nkt = ((long long)M + fa::kPrefillTile - 1) / fa::kPrefillTile;
+    if (nkt * B * Hkv > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != FA_OK) return s;
+    const size_t acc_elems = (size_t)B * N * Hq * d;
+    const size_t bytes = (acc_elems + (size_t)B * Hq * N) * sizeof(float);
+    void* ws = nullptr;
+    if ((s = workspace(st, (cudaStream_t)stream, bytes, &ws)) != FA_OK) return s;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((s = encode_map(&tq, q, dtype, d, Hq, N, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
+    if ((s = encode_map(&tk, k, dtype, d, Hkv, M, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
+    if ((s = encode_map(&tv, v, dtype, d, Hkv, M, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
+    if ((s = encode_map(&tdo, dout, dtype, d, Hq, N, B, 64, fa::kPrefillTile, true)) != FA_OK)
+        return s;
+    fa::BackwardArgs a{};
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq_acc = static_cast<float*>(ws);
+    a.dsum = static_cast<float*>(ws) + acc_elems;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.M = M;
+    a.causal = causal;
+    a.n_qtiles = (N + fa::kPrefillTile - 1) / fa::kPrefillTile;
+    a.n_ktiles = (int)nkt;
+    a.scale = scale;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.status = st->status;
+    a.timeout_ns = g_timeout_ns.load();
+    return from_cuda(fa::launch_backward(tq, tk, tv, tdo, a, d, (int)dtype, (cudaStream_t)stream));
+}
+
 FA_EXPORT fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int Hq, int Hkv, int M, int d, int chunk, float scale,
                               fa_dtype dtype, fa_stream_t stream) {

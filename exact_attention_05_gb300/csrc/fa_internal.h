@@ -78,6 +78,31 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const CUtensorMap& to, const PrefillArgs& a, int d, int dtype,
                            cudaStream_t stream);
 
+// Backward (dQ, dK, dV).  Tensors as in the forward; lse [B, Hq, N] natural
+// log (as fa_fwd writes it); dsum [B, Hq, N] fp32 and dq_acc [B, N, Hq, d]
+// fp32 are workspace.
+struct BackwardArgs {
+    const void* o;         // [B, N, Hq, d] forward output
+    const void* dout;      // [B, N, Hq, d]
+    const float* lse;      // [B, Hq, N]
+    float* dsum;           // [B, Hq, N]: D_i = dO_i . O_i
+    float* dq_acc;         // [B, N, Hq, d] fp32 accumulator of dQ / scale
+    void* dq;              // [B, N, Hq, d]
+    void* dk;              // [B, M, Hkv, d]
+    void* dv;              // [B, M, Hkv, d]
+    int B, Hq, Hkv, N, M;
+    int causal;
+    int n_qtiles, n_ktiles;
+    float scale, scale_log2;
+    int* status;
+    unsigned long long timeout_ns;
+};
+
+// tq/tdo over [B, N, Hq, d], tk/tv over [B, M, Hkv, d]: 64 x 128-row boxes, 128-byte swizzle.
+cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BackwardArgs& a, int d, int dtype,
+                            cudaStream_t stream);
+
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int d,
                           int dtype, cudaStream_t stream);
 

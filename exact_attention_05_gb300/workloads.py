@@ -193,6 +193,13 @@ def make_inputs(B, Hq, Hkv, N, M, d, dtype, seed, peaky_frac=0.0):
     return q.to(tdt), k.to(tdt), v.to(tdt)
 
 
+def make_dout(B, N, Hq, d, dtype, seed):
+    """Upstream gradient dO [B, N, Hq, d] for the backward: iid N(0, 1) float32
+    from its own generator, rounded to the 16-bit dtype."""
+    g = torch.Generator().manual_seed(int(seed))
+    return torch.randn((B, N, Hq, d), generator=g, dtype=torch.float32).to(TORCH_DTYPE[dtype])
+
+
 def workload_inputs(w: Workload):
     return make_inputs(w.B, w.Hq, w.Hkv, w.N, w.M, w.d, w.dtype, w.seed, w.peaky_frac)
 

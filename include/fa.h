@@ -160,6 +160,34 @@ fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, void* o
                             float scale, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * Backward of fa_fwd: the gradients dQ, dK, dV of O = softmax(scale Q K^T
+ * [+ causal]) V for an upstream gradient dO.  "Tensor Core 迁移计划" (phase
+ * 2) names the backward's contractions dV = P^T dO, dP = dO V^T and dQ, dK
+ * from dS; dS = P o (dP - D) with D_i = dO_i . O_i is the softmax's Jacobian,
+ * and P is recomputed from the forward's LSE (nothing of size N x M is kept).
+ *
+ *   q, k, v, o   the forward's inputs and output (layouts as fa_fwd).
+ *   lse          device, [B, Hq, N] fp32: the natural-log LSE fa_fwd wrote
+ *                for the same q, k, v, causal and scale (required).
+ *   dout         device, [B, N, Hq, d]: dL/dO, of `dtype`.
+ *   dq           device, [B, N, Hq, d] out; dk, dv device, [B, M, Hkv, d] out,
+ *                of `dtype` (with GQA, dk/dv of a kv head sum over the query
+ *                heads that read it).
+ *   others       as fa_fwd.
+ * P and dS enter the tensor core as fp16/bf16 (as P does in the forward);
+ * every accumulation is fp32.  Three launches on `stream`: D = rowsum(dO o O)
+ * (also zeroing the fp32 dQ accumulator), the main kernel, and the dQ
+ * conversion.  Workspace: B*N*Hq*(d+1) fp32 values in the library's
+ * per-(device, stream) buffer (the one fa_decode uses), allocated or grown on
+ * demand (growing synchronises the device).
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for a NULL or misaligned lse,
+ * dout, dq, dk or dv; FA_ERR_NO_MEMORY if the workspace cannot be allocated.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                 int M, int d, int causal, float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * Split-KV decode over an FP8 (e4m3) K/V cache with one fp32 scale per kv
  * head.  FP8 and INT8/INT4 KV quantisation are named as the next memory-side
  * step in the closing "TODO" section of "[CUDA 优化实战] fmha sm120 : 超越

@@ -61,6 +61,16 @@ def dec(**kw):
                         args["scale"], args["dtype"], stream=0, check=False)
 
 
+def bwd(**kw):
+    args = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=GOOD, do=GOOD, dq=GOOD, dk=GOOD, dv=GOOD, B=1,
+                Hq=2, Hkv=2, N=128, M=128, d=128, causal=0, scale=0.1, dtype=0)
+    args.update(kw)
+    return fa.fa_bwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["do"],
+                     args["dq"], args["dk"], args["dv"], args["B"], args["Hq"], args["Hkv"],
+                     args["N"], args["M"], args["d"], args["causal"], args["scale"], args["dtype"],
+                     stream=0, check=False)
+
+
 def dec8(**kw):
     args = dict(q=GOOD, k=GOOD, v=GOOD, ks=GOOD, vs=GOOD, o=GOOD, lse=None, B=1, Hq=2, Hkv=2,
                 M=128, d=128, chunk=128, scale=0.1, dtype=0)
@@ -80,7 +90,7 @@ def decp(**kw):
                               args["chunk"], args["scale"], args["dtype"], stream=0, check=False)
 
 
-@pytest.mark.parametrize("call", [fwd, dec, dec8, decp])
+@pytest.mark.parametrize("call", [fwd, dec, dec8, decp, bwd])
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), fa.FA_ERR_INVALID_ARG),
     (dict(k=None), fa.FA_ERR_INVALID_ARG),
@@ -142,6 +152,13 @@ def test_invalid_fp8_decode_arguments(lib, kw):
 ])
 def test_invalid_paged_decode_arguments(lib, kw):
     assert decp(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(lse=None), dict(do=None), dict(dq=None), dict(dk=None),
+                                dict(dv=None), dict(do=MIS), dict(dq=MIS), dict(dk=MIS),
+                                dict(dv=MIS), dict(lse=GOOD + 2), dict(causal=2), dict(N=0)])
+def test_invalid_backward_arguments(lib, kw):
+    assert bwd(**kw) == fa.FA_ERR_INVALID_ARG
 
 
 def test_python_binding_raises_with_status(lib):
