@@ -243,7 +243,9 @@ FA_EXPORT fa_status fa_bwd(const void* q, const void* k, const void* v, const vo
     DeviceState* st = nullptr;
     if ((s = device_state(&st)) != FA_OK) return s;
     const size_t acc_elems = (size_t)B * N * Hq * d;
-    const size_t bytes = (acc_elems + (size_t)B * Hq * N) * sizeof(float);
+    const int n_qtiles = (N + fa::kPrefillTile - 1) / fa::kPrefillTile;
+    const size_t pack_elems = (size_t)B * Hq * n_qtiles * 2 * fa::kPrefillTile;
+    const size_t bytes = (acc_elems + pack_elems) * sizeof(float);
     void* ws = nullptr;
     if ((s = workspace(st, (cudaStream_t)stream, bytes, &ws)) != FA_OK) return s;
     CUtensorMap tq, tk, tv, tdo;
@@ -257,7 +259,7 @@ FA_EXPORT fa_status fa_bwd(const void* q, const void* k, const void* v, const vo
     a.dout = dout;
     a.lse = lse;
     a.dq_acc = static_cast<float*>(ws);
-    a.dsum = static_cast<float*>(ws) + acc_elems;
+    a.pack = static_cast<float*>(ws) + acc_elems;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -267,7 +269,7 @@ FA_EXPORT fa_status fa_bwd(const void* q, const void* k, const void* v, const vo
     a.N = N;
     a.M = M;
     a.causal = causal;
-    a.n_qtiles = (N + fa::kPrefillTile - 1) / fa::kPrefillTile;
+    a.n_qtiles = n_qtiles;
     a.n_ktiles = (int)nkt;
     a.scale = scale;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);

@@ -9,6 +9,7 @@
 
 // Low byte of the device status word; the next byte says which wait expired.
 #define FA_DEV_TIMEOUT 1
+#define FA_DEV_LAYOUT 2   // a kernel found its shared-memory base misaligned
 
 // Where a bounded wait sits (recorded in bits 8.. of the status word).
 enum FaWaitSite {
@@ -21,6 +22,7 @@ enum FaWaitSite {
     FA_SITE_DRAIN = 7,
     FA_SITE_DECODE_KV = 8,
     FA_SITE_SELFTEST = 9,
+    FA_SITE_SMEM_ALIGN = 10,
 };
 
 namespace fa {
@@ -79,13 +81,12 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            cudaStream_t stream);
 
 // Backward (dQ, dK, dV).  Tensors as in the forward; lse [B, Hq, N] natural
-// log (as fa_fwd writes it); dsum [B, Hq, N] fp32 and dq_acc [B, N, Hq, d]
-// fp32 are workspace.
+// log (as fa_fwd writes it); pack and dq_acc [B, N, Hq, d] fp32 are workspace.
 struct BackwardArgs {
     const void* o;         // [B, N, Hq, d] forward output
     const void* dout;      // [B, N, Hq, d]
     const float* lse;      // [B, Hq, N]
-    float* dsum;           // [B, Hq, N]: D_i = dO_i . O_i
+    float* pack;           // [B, Hq, n_qtiles, 2, 128]: LSE*log2(e) (+inf past N), then D_i = dO_i . O_i
     float* dq_acc;         // [B, N, Hq, d] fp32 accumulator of dQ / scale
     void* dq;              // [B, N, Hq, d]
     void* dk;              // [B, M, Hkv, d]
