@@ -254,6 +254,20 @@ FA_EXPORT fa_status fa_bwd(const void* q, const void* k, const void* v, const vo
     if ((s = encode_map(&tv, v, dtype, d, Hkv, M, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
     if ((s = encode_map(&tdo, dout, dtype, d, Hq, N, B, 64, fa::kPrefillTile, true)) != FA_OK)
         return s;
+    // fp32 dQ accumulator [B, N, Hq, d], the target of the kernel's bulk reductions
+    CUtensorMap tdq;
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)N, (cuuint64_t)B};
+        const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)Hq * d * 4,
+                                       (cuuint64_t)N * Hq * d * 4};
+        const cuuint32_t box[4] = {32, 1, (cuuint32_t)fa::kPrefillTile, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return FA_ERR_CUDA;
+    }
     fa::BackwardArgs a{};
     a.o = o;
     a.dout = dout;
@@ -275,7 +289,8 @@ FA_EXPORT fa_status fa_bwd(const void* q, const void* k, const void* v, const vo
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.status = st->status;
     a.timeout_ns = g_timeout_ns.load();
-    return from_cuda(fa::launch_backward(tq, tk, tv, tdo, a, d, (int)dtype, (cudaStream_t)stream));
+    return from_cuda(
+        fa::launch_backward(tq, tk, tv, tdo, tdq, a, d, (int)dtype, (cudaStream_t)stream));
 }
 
 FA_EXPORT fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -76,7 +76,8 @@ struct BwdCfg {
     static constexpr int B_DQ = 8;       // dQ in TMEM (and every earlier MMA done)
     static constexpr int B_DQFREE = 9;   // dQ read out of TMEM (256 arrivals)
     static constexpr int B_FINAL = 10;   // every MMA done: dK, dV final
-    static constexpr int NBAR = 11;
+    static constexpr int B_CSYNC = 11;   // barrier among the compute threads (256 arrivals)
+    static constexpr int NBAR = 12;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     // The dynamic shared-memory base is 1 KB aligned (checked at run time), so
     // no alignment slack is allocated: the layout needs all but ~1 KB of the
@@ -149,10 +150,16 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const BackwardArgs a, l
     reinterpret_cast<uint2*>(a.dq)[i] = make_uint2(pack2<T>(v.x * s, v.y * s), pack2<T>(v.z * s, v.w * s));
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
+// TMA bulk reduction: the box at `src` (shared) is added element-wise (fp32)
+// into the tensor at the given coordinates; rows past the tensor's end are
+// dropped.  Tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, uint32_t src, int c0,
+                                                  int c1, int c2, int c3) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], "
+        "[%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
 }
 
 // Plain (non-tensor) bulk copy global -> shared, completing on `bar`.  Both
@@ -170,7 +177,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BackwardArgs a) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BackwardArgs a) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
@@ -214,6 +221,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(C::B_DQ), 1);
         mbar_init(bar(C::B_DQFREE), kComputeThreads);
         mbar_init(bar(C::B_FINAL), 1);
+        mbar_init(bar(C::B_CSYNC), kComputeThreads);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -222,6 +230,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         prefetch_tensor_map(&tm_k);
         prefetch_tensor_map(&tm_v);
         prefetch_tensor_map(&tm_do);
+        prefetch_tensor_map(&tm_dq);
     }
     if (warp == 9) {
         tmem_alloc(smem_addr(const_cast<uint32_t*>(tmem_holder)), C::TMEM_COLS);
@@ -356,6 +365,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool kvalid = key < a.M;
         const float sl2 = a.scale_log2;
         constexpr int HD = D / 2;  // dQ / dV / dK columns per warpgroup
+        // Barrier among the 256 compute threads on an mbarrier, so that its wait
+        // is bounded like every other (a warp that gave up never strands the rest).
+        uint32_t csync_uses = 0;
+        auto csync = [&]() -> bool {
+            mbar_arrive(bar(C::B_CSYNC));
+            const bool got = mbar_wait(bar(C::B_CSYNC), csync_uses & 1u, wc, FA_SITE_SOFTMAX_O);
+            ++csync_uses;
+            return __all_sync(0xffffffffu, got);
+        };
         bool ok = true;
         for (int t = 0; ok && t < ntile; ++t) {
             const int buf = t & 1;
@@ -372,7 +390,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            // ---- P^T = exp2(scale log2e S^T - LSE log2e), masked: 16-bit into TMEM [64 wg, 64 wg + 32)
+            // ---- P^T = exp2(scale log2e S^T - LSE log2e): 16-bit into TMEM [64 wg, 64 wg + 32).
+            // Only a tile that straddles the diagonal needs the causal mask; keys
+            // past M give P = 0 for the whole row; rows past N carry LSE = +inf.
+            const bool diag = a.causal && key0 + C::BN - 1 > i * C::BM;
             float p[64];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -382,16 +403,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_wait_ld();
                 uint32_t pw[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int qg = i * C::BM + qb + e;  // global query row
-                    const bool v0 = kvalid && (!a.causal || key <= qg);
-                    const bool v1 = kvalid && (!a.causal || key <= qg + 1);
-                    // rows past N carry LSE = +inf, so their P is exp2(-inf) = 0
-                    p[32 * c + e] = v0 ? fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -lse2[qb + e])) : 0.f;
-                    p[32 * c + e + 1] =
-                        v1 ? fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2[qb + e + 1])) : 0.f;
-                    pw[e / 2] = pack2<T>(p[32 * c + e], p[32 * c + e + 1]);
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(lse2 + qb + e);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        p[32 * c + e + u] = fast_exp2(fmaf(__uint_as_float(sv[e + u]), sl2, -lv[u]));
                 }
+                if (diag || !kvalid) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int qg = i * C::BM + qb + e;  // global query row
+                        if (!kvalid || key > qg) p[32 * c + e] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) pw[e / 2] = pack2<T>(p[32 * c + e], p[32 * c + e + 1]);
                 tmem_st16(lane_base + C::TM_S + 64 * wg + 16 * c, pw);
             }
             got = mbar_wait(bar(C::B_DP), t & 1, wc, FA_SITE_SOFTMAX_S);
@@ -400,6 +427,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             }
             tc_fence_after();
+            // the dS buffer doubled as the previous tile's dQ staging: its bulk
+            // reductions must have read it before it is overwritten
+            if (threadIdx.x == 0) tma_store_wait_all();
+            if (!csync()) {
+                ok = false;
+                break;
+            }
             // ---- dS^T = P^T (dP^T - D): 16-bit into TMEM [128 + 64 wg, +32) and into
             // smem as dS [query half wg][key row r][64 queries], 128-byte swizzled
 #pragma unroll
@@ -410,10 +444,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_wait_ld();
                 uint32_t dw[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float d0 = p[32 * c + e] * (__uint_as_float(dv[e]) - dsum[qb + e]);
-                    const float d1 = p[32 * c + e + 1] * (__uint_as_float(dv[e + 1]) - dsum[qb + e + 1]);
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4*>(dsum + qb + e);
+                    const float d0 = p[32 * c + e] * (__uint_as_float(dv[e]) - d4.x);
+                    const float d1 = p[32 * c + e + 1] * (__uint_as_float(dv[e + 1]) - d4.y);
+                    const float d2 = p[32 * c + e + 2] * (__uint_as_float(dv[e + 2]) - d4.z);
+                    const float d3 = p[32 * c + e + 3] * (__uint_as_float(dv[e + 3]) - d4.w);
                     dw[e / 2] = pack2<T>(d0, d1);
+                    dw[e / 2 + 1] = pack2<T>(d2, d3);
                 }
                 tmem_st16(lane_base + C::TM_DP + 64 * wg + 16 * c, dw);
 #pragma unroll
@@ -428,31 +466,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             fence_async_shared();  // the tensor core reads dS through the async proxy
             tc_fence_before();
             mbar_arrive(bar(C::B_P));
-            // ---- dQ (query row r, columns [wg d/2, wg d/2 + d/2)) -> fp32 accumulator
+            // ---- dQ (query row r) -> fp32 accumulator: staged through the dS buffer
+            // (free once the dQ MMA has read it) in 128-byte-swizzled boxes of 32
+            // columns x 128 rows, then added by TMA bulk reductions, which reduce
+            // whole lines in L2 (row-per-thread global atomics do not coalesce).
             got = mbar_wait(bar(C::B_DQ), t & 1, wc, FA_SITE_SOFTMAX_O);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int q = i * C::BM + r;
-            float* dst = a.dq_acc + ((size_t(b) * a.N + q) * a.Hq + h) * D + wg * HD;
+            constexpr int ROUNDS = D / 64;  // 64 columns (two boxes, 32 KB) per round
 #pragma unroll 1
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int rd = 0; rd < ROUNDS; ++rd) {
+                if (rd > 0) {
+                    // the previous round's boxes must have been read out of the buffer
+                    if (threadIdx.x == 0) tma_store_wait_all();
+                    if (!csync()) {
+                        ok = false;
+                        break;
+                    }
+                }
                 uint32_t v[32];
-                tmem_ld32(lane_base + C::TM_DQ + wg * HD + c * 32, v);
+                tmem_ld32(lane_base + C::TM_DQ + 64 * rd + 32 * wg, v);
                 tmem_wait_ld();
-                if (q < a.N) {
+                uint8_t* box = smem + C::DS_OFF + wg * C::SUB_BYTES;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        red_add_v4(dst + c * 32 + 4 * u, __uint_as_float(v[4 * u]),
-                                   __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
-                                   __uint_as_float(v[4 * u + 3]));
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4*>(box + r * 128 + ((u ^ (r & 7)) << 4)) =
+                        make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                fence_async_shared();
+                if (!csync()) {
+                    ok = false;
+                    break;
+                }
+                if (threadIdx.x == 0) {
+                    for (int w = 0; w < 2; ++w)
+                        tma_reduce_add_4d(&tm_dq, sbase + C::DS_OFF + w * C::SUB_BYTES,
+                                          64 * rd + 32 * w, h, i * C::BM, b);
+                    tma_store_commit();
                 }
             }
+            if (!ok) break;
             tc_fence_before();
             mbar_arrive(bar(C::B_DQFREE));
         }
+        // the last tile's bulk reductions must have read their boxes before the CTA exits
+        if (threadIdx.x == 0) tma_store_wait_all();
         // ---- dK (times scale) and dV of this CTA's keys: key row r, columns
         // [wg d/2, wg d/2 + d/2).  tcgen05.ld is warp-collective: every lane loads,
         // whether or not its key exists; only the stores depend on it.
@@ -504,7 +564,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, typename T>
 cudaError_t launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BackwardArgs& a, cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BackwardArgs& a,
+                       cudaStream_t stream) {
     using C = BwdCfg<D>;
     const long long prow = (long long)a.B * a.Hq * a.n_qtiles * 128;
     const long long nb0 = (prow + 7) / 8;
@@ -517,7 +578,7 @@ cudaError_t launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (err != cudaSuccess) return err;
     const long long nblocks = (long long)a.n_ktiles * a.B * a.Hkv;
     if (nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<dim3((unsigned)nblocks), dim3(kBwdThreads), C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, a);
+    kern<<<dim3((unsigned)nblocks), dim3(kBwdThreads), C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const long long n4 = (long long)a.B * a.N * a.Hq * D / 4;
     dq_convert_kernel<T><<<dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, stream>>>(a, n4);
@@ -527,14 +588,14 @@ cudaError_t launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 }  // namespace
 
 cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BackwardArgs& a, int d, int dtype,
-                            cudaStream_t stream) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BackwardArgs& a,
+                            int d, int dtype, cudaStream_t stream) {
     if (d == 128)
-        return dtype == 0 ? launch_all<128, __half>(tq, tk, tv, tdo, a, stream)
-                          : launch_all<128, __nv_bfloat16>(tq, tk, tv, tdo, a, stream);
+        return dtype == 0 ? launch_all<128, __half>(tq, tk, tv, tdo, tdq, a, stream)
+                          : launch_all<128, __nv_bfloat16>(tq, tk, tv, tdo, tdq, a, stream);
     if (d == 64)
-        return dtype == 0 ? launch_all<64, __half>(tq, tk, tv, tdo, a, stream)
-                          : launch_all<64, __nv_bfloat16>(tq, tk, tv, tdo, a, stream);
+        return dtype == 0 ? launch_all<64, __half>(tq, tk, tv, tdo, tdq, a, stream)
+                          : launch_all<64, __nv_bfloat16>(tq, tk, tv, tdo, tdq, a, stream);
     return cudaErrorInvalidValue;
 }
 

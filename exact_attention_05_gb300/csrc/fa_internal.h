@@ -99,10 +99,12 @@ struct BackwardArgs {
     unsigned long long timeout_ns;
 };
 
-// tq/tdo over [B, N, Hq, d], tk/tv over [B, M, Hkv, d]: 64 x 128-row boxes, 128-byte swizzle.
+// tq/tdo over [B, N, Hq, d], tk/tv over [B, M, Hkv, d]: 64 x 128-row boxes, 128-byte
+// swizzle; tdq over the fp32 dQ accumulator [B, N, Hq, d]: 32 x 128-row boxes, 128-byte
+// swizzle (the target of bulk reductions).
 cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BackwardArgs& a, int d, int dtype,
-                            cudaStream_t stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BackwardArgs& a,
+                            int d, int dtype, cudaStream_t stream);
 
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int d,
                           int dtype, cudaStream_t stream);
