@@ -36,7 +36,11 @@
 //      overwrite operands that earlier MMAs read: tcgen05 MMAs issued by one
 //      thread execute in issue order.
 //        warps 0-7 compute; warp 8 TMA producer; warp 9 TMEM allocator and
-//        single-thread MMA issuer.
+//        single-thread MMA issuer; warp 10 issues the dQ bulk reductions.
+//      dQ is read out of TMEM, staged in this tile's Q and dO slots (dead once
+//      dK and dV have read them) as 128-byte-swizzled fp32 boxes, and added to
+//      the fp32 accumulator by TMA bulk reductions, which reduce whole lines in
+//      L2; the slots are refilled once the reductions have read them.
 //   3. dq_convert_kernel: dQ = scale * accumulator, rounded to the input type.
 // Every wait is bounded; on expiry the CTA records the timeout, drains its own
 // copies and MMAs, frees TMEM and returns.
@@ -76,8 +80,9 @@ struct BwdCfg {
     static constexpr int B_DQ = 8;       // dQ in TMEM (and every earlier MMA done)
     static constexpr int B_DQFREE = 9;   // dQ read out of TMEM (256 arrivals)
     static constexpr int B_FINAL = 10;   // every MMA done: dK, dV final
-    static constexpr int B_CSYNC = 11;   // barrier among the compute threads (256 arrivals)
-    static constexpr int NBAR = 12;
+    static constexpr int B_STAGEFULL = 11;  // dQ staged in the tile's Q/dO slots (256 arrivals)
+    static constexpr int B_STAGED = 12;     // [2] the staged dQ of a buffer has been read out
+    static constexpr int NBAR = 14;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     // The dynamic shared-memory base is 1 KB aligned (checked at run time), so
     // no alignment slack is allocated: the layout needs all but ~1 KB of the
@@ -89,7 +94,7 @@ struct BwdCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 constexpr int kComputeThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -221,7 +226,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(C::B_DQ), 1);
         mbar_init(bar(C::B_DQFREE), kComputeThreads);
         mbar_init(bar(C::B_FINAL), 1);
-        mbar_init(bar(C::B_CSYNC), kComputeThreads);
+        mbar_init(bar(C::B_STAGEFULL), kComputeThreads);
+        mbar_init(bar(C::B_STAGED), 1);
+        mbar_init(bar(C::B_STAGED + 1), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -253,9 +260,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             int t = 0;
             for (; t < ntile; ++t) {
                 const int buf = t & 1;
-                // the tile two back used this buffer
-                if (t >= 2 && !mbar_wait(bar(C::B_QFREE + buf), ((t - 2) >> 1) & 1, wc,
-                                         FA_SITE_PRODUCER_SLOT))
+                // the tile two back used this buffer: its MMAs, and its dQ staging in
+                // the dO slot, must be done with it
+                if (t >= 2 && (!mbar_wait(bar(C::B_QFREE + buf), ((t - 2) >> 1) & 1, wc,
+                                          FA_SITE_PRODUCER_SLOT) ||
+                               !mbar_wait(bar(C::B_STAGED + buf), ((t - 2) >> 1) & 1, wc,
+                                          FA_SITE_PRODUCER_SLOT)))
                     break;
                 int h, i;
                 tile_of(t, h, i);
@@ -353,6 +363,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(bar(C::B_FINAL));
             mbar_drain_wait(bar(C::B_FINAL), 0, wc, FA_SITE_DRAIN);
         }
+    } else if (warp == 10) {
+        // ------------------------------------------------------------- reducer
+        if (lane == 0) {
+            for (int t = 0; t < ntile; ++t) {
+                if (!mbar_wait(bar(C::B_STAGEFULL), t & 1, wc, FA_SITE_SOFTMAX_O)) break;
+                const int buf = t & 1;
+                int h, i;
+                tile_of(t, h, i);
+                for (int k = 0; k < D / 32; ++k)
+                    tma_reduce_add_4d(&tm_dq,
+                                      sbase + (k < C::NSUB ? C::Q_OFF + k * C::SUB_BYTES
+                                                           : C::DO_OFF + (k - C::NSUB) * C::SUB_BYTES) +
+                                          buf * C::TILE_BYTES,
+                                      32 * k, h, i * C::BM, b);
+                tma_store_commit();
+                // once the boxes are read the slots may be refilled (and the CTA may exit)
+                tma_store_wait_all();
+                mbar_arrive(bar(C::B_STAGED + buf));
+            }
+        }
     } else {
         // ------------------------------------------------------------ compute
         // thread <-> TMEM lane r (key row for S^T, dP^T, dV, dK; query row for
@@ -365,15 +395,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool kvalid = key < a.M;
         const float sl2 = a.scale_log2;
         constexpr int HD = D / 2;  // dQ / dV / dK columns per warpgroup
-        // Barrier among the 256 compute threads on an mbarrier, so that its wait
-        // is bounded like every other (a warp that gave up never strands the rest).
-        uint32_t csync_uses = 0;
-        auto csync = [&]() -> bool {
-            mbar_arrive(bar(C::B_CSYNC));
-            const bool got = mbar_wait(bar(C::B_CSYNC), csync_uses & 1u, wc, FA_SITE_SOFTMAX_O);
-            ++csync_uses;
-            return __all_sync(0xffffffffu, got);
-        };
         bool ok = true;
         for (int t = 0; ok && t < ntile; ++t) {
             const int buf = t & 1;
@@ -427,13 +448,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            // the dS buffer doubled as the previous tile's dQ staging: its bulk
-            // reductions must have read it before it is overwritten
-            if (threadIdx.x == 0) tma_store_wait_all();
-            if (!csync()) {
-                ok = false;
-                break;
-            }
             // ---- dS^T = P^T (dP^T - D): 16-bit into TMEM [128 + 64 wg, +32) and into
             // smem as dS [query half wg][key row r][64 queries], 128-byte swizzled
 #pragma unroll
@@ -466,53 +480,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             fence_async_shared();  // the tensor core reads dS through the async proxy
             tc_fence_before();
             mbar_arrive(bar(C::B_P));
-            // ---- dQ (query row r) -> fp32 accumulator: staged through the dS buffer
-            // (free once the dQ MMA has read it) in 128-byte-swizzled boxes of 32
-            // columns x 128 rows, then added by TMA bulk reductions, which reduce
-            // whole lines in L2 (row-per-thread global atomics do not coalesce).
+            // ---- dQ (query row r) -> fp32 accumulator.  The row's columns of this
+            // warpgroup are read out of TMEM first, so that dP^T(t+1) may overwrite
+            // them at once, then staged as box k = columns [32k, 32k + 32) in the Q
+            // slot (boxes 0 .. NSUB-1) and the dO slot (the rest) of this tile; the
+            // reducer warp adds them to the accumulator.
             got = mbar_wait(bar(C::B_DQ), t & 1, wc, FA_SITE_SOFTMAX_O);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            constexpr int ROUNDS = D / 64;  // 64 columns (two boxes, 32 KB) per round
-#pragma unroll 1
-            for (int rd = 0; rd < ROUNDS; ++rd) {
-                if (rd > 0) {
-                    // the previous round's boxes must have been read out of the buffer
-                    if (threadIdx.x == 0) tma_store_wait_all();
-                    if (!csync()) {
-                        ok = false;
-                        break;
-                    }
-                }
-                uint32_t v[32];
-                tmem_ld32(lane_base + C::TM_DQ + 64 * rd + 32 * wg, v);
-                tmem_wait_ld();
-                uint8_t* box = smem + C::DS_OFF + wg * C::SUB_BYTES;
+            constexpr int NB = HD / 32;  // boxes per warpgroup
+            uint32_t v[NB][32];
+#pragma unroll
+            for (int x = 0; x < NB; ++x) tmem_ld32(lane_base + C::TM_DQ + 32 * (wg * NB + x), v[x]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_DQFREE));
+#pragma unroll
+            for (int x = 0; x < NB; ++x) {
+                const int k = wg * NB + x;
+                uint8_t* box = smem + (k < C::NSUB ? C::Q_OFF + k * C::SUB_BYTES
+                                                   : C::DO_OFF + (k - C::NSUB) * C::SUB_BYTES) +
+                               buf * C::TILE_BYTES;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     *reinterpret_cast<uint4*>(box + r * 128 + ((u ^ (r & 7)) << 4)) =
-                        make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-                fence_async_shared();
-                if (!csync()) {
-                    ok = false;
-                    break;
-                }
-                if (threadIdx.x == 0) {
-                    for (int w = 0; w < 2; ++w)
-                        tma_reduce_add_4d(&tm_dq, sbase + C::DS_OFF + w * C::SUB_BYTES,
-                                          64 * rd + 32 * w, h, i * C::BM, b);
-                    tma_store_commit();
-                }
+                        make_uint4(v[x][4 * u], v[x][4 * u + 1], v[x][4 * u + 2], v[x][4 * u + 3]);
             }
-            if (!ok) break;
-            tc_fence_before();
-            mbar_arrive(bar(C::B_DQFREE));
+            fence_async_shared();  // the reductions read the boxes through the async proxy
+            mbar_arrive(bar(C::B_STAGEFULL));
         }
-        // the last tile's bulk reductions must have read their boxes before the CTA exits
-        if (threadIdx.x == 0) tma_store_wait_all();
         // ---- dK (times scale) and dV of this CTA's keys: key row r, columns
         // [wg d/2, wg d/2 + d/2).  tcgen05.ld is warp-collective: every lane loads,
         // whether or not its key exists; only the stores depend on it.
