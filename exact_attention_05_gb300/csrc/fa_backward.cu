@@ -76,13 +76,14 @@ struct BwdCfg {
     static constexpr int B_QFREE = 3;    // [2] the MMAs reading a buffer are done
     static constexpr int B_S = 5;        // S^T in TMEM
     static constexpr int B_DP = 6;       // dP^T in TMEM
-    static constexpr int B_P = 7;        // P^T, dS^T in TMEM and dS in smem (256 arrivals)
+    static constexpr int B_DS = 7;       // dS^T in TMEM and dS in smem (256 arrivals)
     static constexpr int B_DQ = 8;       // dQ in TMEM (and every earlier MMA done)
     static constexpr int B_DQFREE = 9;   // dQ read out of TMEM (256 arrivals)
     static constexpr int B_FINAL = 10;   // every MMA done: dK, dV final
     static constexpr int B_STAGEFULL = 11;  // dQ staged in the tile's Q/dO slots (256 arrivals)
     static constexpr int B_STAGED = 12;     // [2] the staged dQ of a buffer has been read out
-    static constexpr int NBAR = 14;
+    static constexpr int B_PT = 14;         // P^T in TMEM (256 arrivals)
+    static constexpr int NBAR = 15;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     // The dynamic shared-memory base is 1 KB aligned (checked at run time), so
     // no alignment slack is allocated: the layout needs all but ~1 KB of the
@@ -222,7 +223,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(bar(C::B_S), 1);
         mbar_init(bar(C::B_DP), 1);
-        mbar_init(bar(C::B_P), kComputeThreads);
+        mbar_init(bar(C::B_DS), kComputeThreads);
+        mbar_init(bar(C::B_PT), kComputeThreads);
         mbar_init(bar(C::B_DQ), 1);
         mbar_init(bar(C::B_DQFREE), kComputeThreads);
         mbar_init(bar(C::B_FINAL), 1);
@@ -338,16 +340,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss(tmem + C::TM_DP, v_k + koff(kk), do_k0 + bstep + koff(kk), id_kk,
                            kk > 0 ? 1u : 0u);
                 mma_commit(bar(C::B_DP));
-                if (!mbar_wait_spin(bar(C::B_P), t & 1, wc, FA_SITE_MMA_P)) {
+                // dV += P^T dO as soon as P^T is there (it overlaps the forming of dS),
+                // then dK += dS^T Q  (M = keys, N = d, K = queries; A in TMEM)
+                if (!mbar_wait_spin(bar(C::B_PT), t & 1, wc, FA_SITE_MMA_P)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // dV += P^T dO, dK += dS^T Q  (M = keys, N = d, K = queries; A in TMEM)
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     mma_ts(tmem + C::TM_DV, tmem + C::TM_S + pcol(kk), do_m0 + bstep + moff(kk), id_ts,
                            (t > 0 || kk > 0) ? 1u : 0u);
+                if (!mbar_wait_spin(bar(C::B_DS), t & 1, wc, FA_SITE_MMA_P)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     mma_ts(tmem + C::TM_DK, tmem + C::TM_DP + pcol(kk), q_m0 + bstep + moff(kk), id_ts,
@@ -442,6 +450,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int e = 0; e < 32; e += 2) pw[e / 2] = pack2<T>(p[32 * c + e], p[32 * c + e + 1]);
                 tmem_st16(lane_base + C::TM_S + 64 * wg + 16 * c, pw);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PT));
             got = mbar_wait(bar(C::B_DP), t & 1, wc, FA_SITE_SOFTMAX_S);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_wait_st();
             fence_async_shared();  // the tensor core reads dS through the async proxy
             tc_fence_before();
-            mbar_arrive(bar(C::B_P));
+            mbar_arrive(bar(C::B_DS));
             // ---- dQ (query row r) -> fp32 accumulator.  The row's columns of this
             // warpgroup are read out of TMEM first, so that dP^T(t+1) may overwrite
             // them at once, then staged as box k = columns [32k, 32k + 32) in the Q
