@@ -103,8 +103,11 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "prefill_kernel": ["fa_prefill.cu", "fa_device.cuh", "fa_internal.h"],
-    "decode_chunk_kernel": ["fa_decode.cu", "fa_device.cuh", "fa_internal.h"],
-    "decode_merge_kernel": ["fa_decode.cu", "fa_device.cuh", "fa_internal.h"],
+    "decode_chunk_kernel": ["fa_decode_kernel.cuh", "fa_decode.cu", "fa_device.cuh",
+                            "fa_internal.h"],
+    "decode_merge_kernel": ["fa_decode_kernel.cuh", "fa_decode.cu", "fa_device.cuh",
+                            "fa_internal.h"],
+    "backward_kernel": ["fa_backward.cu", "fa_device.cuh", "fa_internal.h"],
 }
 
 
@@ -472,6 +475,10 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=headline_ok,
                     help="the timed workload (the FP8 and paged decode workloads are timed "
                          "in the per-workload table)")
+    ap.add_argument("--profile", choices=["prefill", "backward", "decode"], default=None,
+                    help="run only --warmup + --steps calls of one operation on --workload "
+                         "(or the long decode workload) and print nothing else: the "
+                         "command the ncu summaries under profiles/ are taken with")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table, decode line and CPU baseline")
     args = ap.parse_args(argv)
@@ -506,6 +513,18 @@ def main(argv=None):
         flush_ctr[0] = (flush_ctr[0] + 1) & 0xFF
         flush_buf.fill_(flush_ctr[0])
         flush_read.max()
+
+    if args.profile is not None:
+        wp = WORKLOADS[DECODE] if args.profile == "decode" and w.kind != "decode" else w
+        fn = {"prefill": bench_prefill, "backward": bench_backward,
+              "decode": bench_decode}[args.profile]
+        times = fn(torch, fa, wp, args.steps, args.warmup, flush, dist)
+        if rank == 0:
+            print(f"profile {args.profile} {wp.name}: {len(times)} timed calls, "
+                  f"median {statistics.median(times) * 1e3:.1f} us", flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
 
     is_decode = w.kind == "decode"
     # work units of one step: FLOPs (prefill) or HBM bytes (decode), and their scale
