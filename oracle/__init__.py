@@ -82,6 +82,9 @@ def _load():
         lib.oracle_attention_backward.argtypes = [u16p, u16p, u16p, u16p, I, I, I, I, I, I, I,
                                                   I, D, f64p, f64p, f64p]
         lib.oracle_attention_backward.restype = I
+        lib.oracle_attention_backward_dq_rows.argtypes = [u16p, u16p, u16p, u16p, I, I, I, I, I,
+                                                          I, I, I, D, i64p, I, f64p]
+        lib.oracle_attention_backward_dq_rows.restype = I
         u8p = ctypes.POINTER(ctypes.c_uint8)
         f32p = ctypes.POINTER(ctypes.c_float)
         i32p = ctypes.POINTER(ctypes.c_int32)
@@ -223,6 +226,26 @@ def attention_backward(q, k, v, dout, dtype, causal, scale):
     if rc != 0:
         raise ValueError("oracle_attention_backward rejected its arguments")
     return dq, dk, dv
+
+
+def attention_backward_dq_rows(q, k, v, dout, dtype, causal, scale, rows):
+    """dQ of selected query rows: ``rows`` is an int array [R, 3] of (b, h, i).
+    Returns dQ [R, d] fp64 (the same definition as attention_backward)."""
+    lib = _load()
+    B, N, Hq, d = q.shape
+    _, M, Hkv, _ = k.shape
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    dout, dp = _u16(dout)
+    rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+    out = np.zeros((rows.shape[0], d), np.float64)
+    rc = lib.oracle_attention_backward_dq_rows(
+        qp, kp, vp, dp, int(dtype), B, Hq, Hkv, N, M, d, int(bool(causal)), float(scale),
+        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.shape[0], _f64(out))
+    if rc != 0:
+        raise ValueError("oracle_attention_backward_dq_rows rejected its arguments")
+    return out
 
 
 def e4m3(bits: np.ndarray) -> np.ndarray:

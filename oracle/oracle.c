@@ -429,6 +429,84 @@ int oracle_attention_backward(const uint16_t* q, const uint16_t* k, const uint16
     return failed ? -1 : 0;
 }
 
+/*
+ * dQ of the backward above for selected query rows only (sampled checks at
+ * sizes where the full backward would take too long): dQ_i depends on row i
+ * alone -- its P row, dP row and dS row -- so each listed row is the same
+ * definition as in oracle_attention_backward.  rows holds nrows triples
+ * (b, h, i); dq_rows [nrows, d] fp64.
+ */
+int oracle_attention_backward_dq_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                      const uint16_t* dout, int dtype, int B, int Hq, int Hkv,
+                                      int N, int M, int d, int causal, double scale,
+                                      const int64_t* rows, int nrows, double* dq_rows) {
+    if (check_shape(B, Hq, Hkv, N, M, d) || nrows < 0) return -1;
+    const int g = Hq / Hkv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int rI = 0; rI < nrows; ++rI) {
+        const int64_t b = rows[3 * rI], h = rows[3 * rI + 1], i = rows[3 * rI + 2];
+        if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= N) {
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        const int kh = (int)h / g;
+        const int nk = keys_visible((int)i, M, causal);
+        double* qrow = malloc(sizeof(double) * (size_t)d);
+        double* dorow = malloc(sizeof(double) * (size_t)d);
+        double* krow = malloc(sizeof(double) * (size_t)d);
+        double* vrow = malloc(sizeof(double) * (size_t)d);
+        double* P = malloc(sizeof(double) * (size_t)nk);
+        double* dP = malloc(sizeof(double) * (size_t)nk);
+        if (!qrow || !dorow || !krow || !vrow || !P || !dP) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+            const size_t row = (((size_t)b * N + i) * Hq + h) * (size_t)d;
+            decode_array(q + row, qrow, (size_t)d, dtype);
+            decode_array(dout + row, dorow, (size_t)d, dtype);
+            double m = -INFINITY;
+            for (int j = 0; j < nk; ++j) {
+                decode_array(k + (((size_t)b * M + j) * Hkv + kh) * (size_t)d, krow, (size_t)d, dtype);
+                decode_array(v + (((size_t)b * M + j) * Hkv + kh) * (size_t)d, vrow, (size_t)d, dtype);
+                double s = 0.0, dp = 0.0;
+                for (int t = 0; t < d; ++t) {
+                    s += qrow[t] * krow[t];
+                    dp += dorow[t] * vrow[t];
+                }
+                P[j] = scale * s;
+                dP[j] = dp;
+                if (P[j] > m) m = P[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < nk; ++j) {
+                P[j] = exp(P[j] - m);
+                l += P[j];
+            }
+            double pdp = 0.0;
+            for (int j = 0; j < nk; ++j) {
+                P[j] /= l;
+                pdp += P[j] * dP[j];
+            }
+            double* out = dq_rows + (size_t)rI * d;
+            for (int t = 0; t < d; ++t) out[t] = 0.0;
+            for (int j = 0; j < nk; ++j) {
+                const double ds = P[j] * (dP[j] - pdp);
+                decode_array(k + (((size_t)b * M + j) * Hkv + kh) * (size_t)d, krow, (size_t)d, dtype);
+                for (int t = 0; t < d; ++t) out[t] += scale * ds * krow[t];
+            }
+        }
+        free(qrow);
+        free(dorow);
+        free(krow);
+        free(vrow);
+        free(P);
+        free(dP);
+    }
+    return failed ? -1 : 0;
+}
+
 /* ---- FP8 (e4m3) K/V --------------------------------------------------------- */
 
 /*

@@ -91,3 +91,43 @@ def test_backward_deterministic_dk_dv():
     b = fa.attention_backward(q, k, v, o, lse, dout, True, 0.088)
     torch.cuda.synchronize()
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("name", ["prefill_causal_gqa32x8_n8192_f16_peaky",
+                                  "prefill_causal_h16_n32768_bf16"])
+def test_backward_workload_full_sampled(oracle_mod, name):
+    """The two large prefill workloads at full size, as the bench runs their backward:
+    dQ on sampled rows against the oracle (dQ_i depends on row i alone), and dK, dV
+    through properties that hold at any size: sum_j dK_j = 0 for every (b, kv head)
+    (the softmax ignores a common shift of the keys), and sum_j dV_j equals the sum of
+    dO over the rows of the query heads that read the kv head (every P row sums to 1).
+    The sums are checked within 8 ulp of the type times sum_j |dK_j| (resp. |dV_j|),
+    the per-element bound added up."""
+    import exact_attention_05_gb300 as fa
+    from exact_attention_05_gb300.workloads import WORKLOADS, sample_rows, workload_inputs
+    torch = torch_cuda()
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w)
+    dout = make_dout(w.B, w.N, w.Hq, w.d, w.dtype, w.seed + 7)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    o, lse = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, w.causal, w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    tol = TOL[w.dtype]
+    rows = sample_rows(w, 96, seed=17)
+    ref = oracle_mod.attention_backward_dq_rows(bits(q), bits(k), bits(v), bits(dout), w.dtype,
+                                                w.causal, w.scale, rows)
+    got = dq.double().cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
+    e = float(np.abs(got - ref).max())
+    assert e <= tol * max(float(np.abs(ref).max()), 1.0), f"dQ rows: {e:.3e}"
+    dk64 = dk.double().cpu().numpy()
+    dv64 = dv.double().cpu().numpy()
+    ksum = np.abs(dk64.sum(axis=1))
+    kbound = tol * np.abs(dk64).sum(axis=1)
+    assert bool((ksum <= kbound + 1e-30).all()), float((ksum / np.maximum(kbound, 1e-30)).max())
+    g = w.Hq // w.Hkv
+    want = dout.double().numpy().reshape(w.B, w.N, w.Hkv, g, w.d).sum(axis=(1, 3))
+    vdiff = np.abs(dv64.sum(axis=1) - want)
+    vbound = tol * np.abs(dv64).sum(axis=1)
+    assert bool((vdiff <= vbound + 1e-30).all()), float((vdiff / np.maximum(vbound, 1e-30)).max())

@@ -136,3 +136,20 @@ def test_backward_invariants(oracle_mod, causal):
     do64 = dout.to(torch.float64).numpy()
     want = do64.reshape(B, N, Hkv, g, d).sum(axis=(1, 3))
     np.testing.assert_allclose(dv.sum(axis=1), want, rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_dq_rows_equal_full_backward(oracle_mod, causal):
+    """The sampled-row dQ used at full size equals the pinned full backward's rows."""
+    gen = torch.Generator().manual_seed(410 + causal)
+    B, N, M, Hq, Hkv, d = 2, 40, 33, 4, 2, 64
+    q = torch.randn((B, N, Hq, d), generator=gen).to(torch.bfloat16)
+    k = torch.randn((B, M, Hkv, d), generator=gen).to(torch.bfloat16)
+    v = torch.randn((B, M, Hkv, d), generator=gen).to(torch.bfloat16)
+    dout = torch.randn((B, N, Hq, d), generator=gen).to(torch.bfloat16)
+    dq, _, _ = oracle_mod.attention_backward(bits(q), bits(k), bits(v), bits(dout), 1, causal, 0.2)
+    rows = np.array([(0, 0, 0), (1, 3, 39), (0, 2, 17), (1, 1, 32), (1, 0, 5)], np.int64)
+    got = oracle_mod.attention_backward_dq_rows(bits(q), bits(k), bits(v), bits(dout), 1, causal,
+                                                0.2, rows)
+    want = np.stack([dq[b, i, h] for b, h, i in rows])
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
