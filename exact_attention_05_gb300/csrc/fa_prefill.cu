@@ -66,7 +66,8 @@ struct PrefillCfg {
     static constexpr int B_PFULL = 3 + 2 * NSLOT;          // one per Q tile
     static constexpr int B_ODONE = 5 + 2 * NSLOT;          // one per Q tile
     static constexpr int B_DRAIN = 7 + 2 * NSLOT;
-    static constexpr int NBAR = 8 + 2 * NSLOT;
+    static constexpr int B_QFULL1 = 8 + 2 * NSLOT;         // Q1 (B_QFULL covers Q0)
+    static constexpr int NBAR = 9 + 2 * NSLOT;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
     // TMEM columns
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
+        mbar_init(bar(C::B_QFULL1), 1);
         for (int i = 0; i < C::NSLOT; ++i) {
             mbar_init(bar(C::B_FULL + i), 1);
             mbar_init(bar(C::B_EMPTY + i), 1);
@@ -152,14 +154,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 8) {
         // ------------------------------------------------------------- producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_QFULL), (t1 ? 2 : 1) * C::TILE_BYTES);
-            for (int i = 0; i < (t1 ? 2 : 1); ++i)
+            // Q0 and K0 first: the first QK needs nothing else; Q1 follows on its own
+            // barrier (the first wave's loads all go out at once, so order matters)
+            auto load_q = [&](int i, uint32_t full) {
+                mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int s = 0; s < C::NSUB; ++s)
-                    tma_load_4d(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q,
-                                s * 64, h, q0 + i * C::BM, b, bar(C::B_QFULL));
+                    tma_load_4d(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64,
+                                h, q0 + i * C::BM, b, full);
+            };
+            load_q(0, bar(C::B_QFULL));
+            bool q1_issued = false;
             int L = 0;  // loads issued: K0, V0, K1, V1, ...
             bool ok = true;
             for (; ok && L < 2 * nt; ++L) {
+                if (L == 1 && t1) {
+                    load_q(1, bar(C::B_QFULL1));
+                    q1_issued = true;
+                }
                 const int slot = L % C::NSLOT;
                 const uint32_t parity = ((L / C::NSLOT) & 1) ^ 1;
                 if (!mbar_wait(bar(C::B_EMPTY + slot), parity, wc, FA_SITE_PRODUCER_SLOT)) {
@@ -175,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Every issued copy must have landed before the CTA may exit.
             mbar_drain_wait(bar(C::B_QFULL), 0, wc, FA_SITE_DRAIN);
+            if (q1_issued) mbar_drain_wait(bar(C::B_QFULL1), 0, wc, FA_SITE_DRAIN);
             for (int slot = 0; slot < C::NSLOT && slot < L; ++slot) {
                 const int last = slot + ((L - 1 - slot) / C::NSLOT) * C::NSLOT;
                 mbar_drain_wait(bar(C::B_FULL + slot), (last / C::NSLOT) & 1, wc, FA_SITE_DRAIN);
@@ -248,7 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 tc_fence_after();
                 qk(0, ks);
-                if (t1) qk(1, ks);
+                if (t1) {
+                    ok = mbar_wait_spin(bar(C::B_QFULL1), 0, wc, FA_SITE_MMA_Q);
+                    if (ok) {
+                        tc_fence_after();
+                        qk(1, ks);
+                    }
+                }
                 release(ks);  // K0
             }
             // Everything a tile's group of MMAs needs (its P, V_j and the next K
