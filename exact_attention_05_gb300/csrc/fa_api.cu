@@ -299,7 +299,7 @@ FA_EXPORT fa_status fa_decode(const void* q, const void* k, const void* v, void*
     fa_status s = check_args(q, k, v, o, lse, B, Hq, Hkv, 1, M, d, scale, (int)dtype);
     if (s != FA_OK) return s;
     if (chunk <= 0) return FA_ERR_INVALID_ARG;
-    if ((long long)B * Hkv > 65535) return FA_ERR_INVALID_ARG;
+    if (((long long)M + chunk - 1) / chunk * B * Hkv > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     const int nc = (int)(((long long)M + chunk - 1) / chunk);
     DeviceState* st = nullptr;
     if ((s = device_state(&st)) != FA_OK) return s;

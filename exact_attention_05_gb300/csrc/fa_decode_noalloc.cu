@@ -122,8 +122,8 @@ FA_EXPORT fa_status fa_decode_noalloc(const void* q, const void* k, const void* 
     if (lse && !aligned(lse, 4)) return FA_ERR_INVALID_ARG;
     if ((uint64_t)B * Hq * d >= kMaxElements || (uint64_t)B * M * Hkv * d >= kMaxElements)
         return FA_ERR_INVALID_ARG;
-    if ((long long)B * Hkv > 65535) return FA_ERR_INVALID_ARG;
     const long long nc = ((long long)M + chunk - 1) / chunk;
+    if (nc * B * Hkv > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     const unsigned long long part_elems = (unsigned long long)B * Hq * nc * d;
     const unsigned long long need = part_elems + (unsigned long long)B * Hq * nc;
     if (need > kScratchFloats) return FA_ERR_SCRATCH_LIMIT;

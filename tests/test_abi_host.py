@@ -128,8 +128,9 @@ def test_invalid_forward_only_arguments(lib, kw):
     assert fwd(**kw) == fa.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("kw", [dict(chunk=0), dict(chunk=-128), dict(B=300, Hq=256, Hkv=256,
-                                                                        M=1, d=64)])
+@pytest.mark.parametrize("kw", [dict(chunk=0), dict(chunk=-128),
+                                dict(B=1 << 16, Hq=1 << 16, Hkv=1 << 16, M=1 << 10, d=64,
+                                     chunk=1)])
 def test_invalid_decode_only_arguments(lib, kw):
     assert dec(**kw) == fa.FA_ERR_INVALID_ARG
 

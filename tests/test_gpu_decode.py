@@ -7,6 +7,7 @@ cases: chunk sizes that do not divide M, chunks of 1 key, chunks longer than
 M or than one 128-key sub-tile, GQA groups larger than one pass (8 heads),
 d = 64, bf16, and M = 1.
 """
+import numpy as np
 import pytest
 
 from exact_attention_05_gb300.workloads import BF16, FP16, WORKLOADS, bits, make_inputs, \
@@ -74,3 +75,17 @@ def test_single_launch_tickets_reset_between_calls(oracle_mod):
             o, lse = run_decode(q, k, v, chunk, 0.1, single_launch=True)
             o_ref, lse_ref = oracle_mod.attention(bits(q), bits(k), bits(v), dtype, False, 0.1)
             assert_close(o, lse, o_ref, lse_ref[:, :, 0], dtype, f"rep {rep} shape {i}")
+
+
+def test_decode_many_sequences(oracle_mod):
+    """B * Hkv = 76,800 (more than a 16-bit grid dimension): the persistent grid
+    takes one CTA per (b, kv head)."""
+    B, Hq, Hkv, M, d = 300, 256, 256, 64, 64
+    q, k, v = make_inputs(B, Hq, Hkv, 1, M, d, FP16, seed=91)
+    o, lse = run_decode(q, k, v, 32, 0.125)
+    rows = np.array([(b, h, 0) for b in (0, 151, 299) for h in (0, 77, 255)], np.int64)
+    o_ref, lse_ref = oracle_mod.attention_rows(bits(q), bits(k), bits(v), FP16, False, 0.125,
+                                               rows)
+    got_o = o[rows[:, 0], 0, rows[:, 1]]
+    got_l = lse[rows[:, 0], rows[:, 1]]
+    assert_close(got_o, got_l, o_ref, lse_ref, FP16, "decode B*Hkv = 76800")
