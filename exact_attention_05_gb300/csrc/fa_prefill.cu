@@ -20,6 +20,7 @@
 //                  writes P (fp16/bf16) back into TMEM over the upper half
 //                  of its S row, rescales its O row when needed, and runs
 //                  the epilogue (O / l -> smem -> TMA store, LSE -> global);
+//                  each warp signals its P with one arrive (after __syncwarp);
 //       warp 8     TMA producer: Q0, Q1 once, then K0, V0, K1, V1, ... into a
 //                  ring of shared-memory slots;
 //       warp 9     TMEM allocator and single-thread tcgen05 MMA issuer.
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < C::NQ; ++i) {
             mbar_init(bar(C::B_SFULL + i), 1);
-            mbar_init(bar(C::B_PFULL + i), 128);
+            mbar_init(bar(C::B_PFULL + i), 4);  // one arrive per softmax warp
             mbar_init(bar(C::B_ODONE + i), 1);
         }
         mbar_init(bar(C::B_DRAIN), 1);
@@ -271,7 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Everything a tile's group of MMAs needs (its P, V_j and the next K
             // tile) is waited for before the group is issued, so that PV_i(j) and
-            // QK_i(j+1) go to the tensor core back to back.
+            // QK_i(j+1) go to the tensor core back to back.  V_j and K_{j+1} are
+            // checked first: they have normally landed long before, and P is the
+            // one wait that is on the critical path, so nothing follows it.
             for (int j = 0; ok && j < nt; ++j) {
                 int nks = ks;
                 uint32_t nkph = kph;
@@ -279,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool next_k = j + 1 < nt;  // some tile still needs K_{j+1}
                 bool have_vk = false;
                 if (j < nt0) {
-                    if (!mbar_wait_spin(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P) ||
-                        !wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph))) {
+                    if (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph)) ||
+                        !mbar_wait_spin(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P)) {
                         ok = false;
                         break;
                     }
@@ -294,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (t1) {
-                    if (!mbar_wait_spin(bar(C::B_PFULL + 1), j & 1, wc, FA_SITE_MMA_P) ||
-                        (!have_vk && (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph))))) {
+                    if ((!have_vk && (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph)))) ||
+                        !mbar_wait_spin(bar(C::B_PFULL + 1), j & 1, wc, FA_SITE_MMA_P)) {
                         ok = false;
                         break;
                     }
@@ -325,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nti = tile == 0 ? nt0 : nt;
         const bool active = tile == 0 || t1;
         const float sl2 = a.scale_log2;
+        // KV tiles [0, jfull) are visible to every row of the tile and lie inside M
+        int jfull = a.M / C::BN;
+        if (a.causal) jfull = min(jfull, row0 / C::BN);
         float m_ref = -INFINITY;  // exponent reference, log2 units of the scaled logits
         float l = 0.f;
         bool ok = active;
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
             }
             const int k0 = j * C::BN;
-            if (k0 + C::BN > a.M || (a.causal && k0 + C::BN - 1 > row0)) {
+            if (j >= jfull) {
                 int lim = a.M - k0;
                 if (a.causal) lim = min(lim, row - k0 + 1);
 #pragma unroll
@@ -423,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL + tile));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_PFULL + tile));
         }
         // ------------------------------------------------------------ epilogue
         if (ok) {
