@@ -42,6 +42,9 @@
 //      the fp32 accumulator by TMA bulk reductions, which reduce whole lines in
 //      L2; the slots are refilled once the reductions have read them.
 //   3. dq_convert_kernel: dQ = scale * accumulator, rounded to the input type.
+// Launches 2 and 3 are programmatic dependents of the launch before them: they
+// may start (set-up, K/V loads) while it finishes, and the threads that read
+// its results wait for it first (griddepcontrol.wait).
 // Every wait is bounded; on expiry the CTA records the timeout, drains its own
 // copies and MMAs, frees TMEM and returns.
 
@@ -105,6 +108,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // zeroes the row's fp32 dQ accumulator.
 template <int D, typename T>
 __global__ void __launch_bounds__(256) dsum_kernel(const BackwardArgs a) {
+    // the backward kernel may start its set-up and K/V loads now; it waits for
+    // this grid to finish before it reads the records or adds into dQ
+    grid_dep_launch_dependents();
     constexpr int EPL = D / 32;  // elements per lane (2 or 4)
     const int nq_pad = a.n_qtiles * 128;
     const long long rows = (long long)a.B * a.Hq * nq_pad;
@@ -149,6 +155,7 @@ __global__ void __launch_bounds__(256) dsum_kernel(const BackwardArgs a) {
 // dQ = scale * accumulator, rounded to T; four elements per thread.
 template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const BackwardArgs a, long long n4) {
+    grid_dep_wait();  // every dQ reduction of the backward kernel has landed
     const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
     if (i >= n4) return;
     const float4 v = reinterpret_cast<const float4*>(a.dq_acc)[i];
@@ -259,6 +266,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_4d(sbase + C::K_OFF + s * C::SUB_BYTES, &tm_k, s * 64, kvh, key0, b, bar(C::B_KV));
                 tma_load_4d(sbase + C::V_OFF + s * C::SUB_BYTES, &tm_v, s * 64, kvh, key0, b, bar(C::B_KV));
             }
+            // the LSE/D records come from the preprocessing kernel
+            grid_dep_wait();
             int t = 0;
             for (; t < ntile; ++t) {
                 const int buf = t & 1;
@@ -374,6 +383,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp == 10) {
         // ------------------------------------------------------------- reducer
         if (lane == 0) {
+            grid_dep_wait();  // the accumulator is zeroed by the preprocessing kernel
             for (int t = 0; t < ntile; ++t) {
                 if (!mbar_wait(bar(C::B_STAGEFULL), t & 1, wc, FA_SITE_SOFTMAX_O)) break;
                 const int buf = t & 1;
@@ -566,6 +576,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // all of this CTA's work is issued: the dQ conversion may launch once every
+    // CTA got here (it waits for the grid to complete before reading dQ)
+    if (threadIdx.x == 0) grid_dep_launch_dependents();
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -588,11 +601,26 @@ cudaError_t launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (err != cudaSuccess) return err;
     const long long nblocks = (long long)a.n_ktiles * a.B * a.Hkv;
     if (nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<dim3((unsigned)nblocks), dim3(kBwdThreads), C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, a);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    // The backward kernel and the dQ conversion are programmatic dependents of
+    // the launch before them: their launch and set-up overlap its tail.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)nblocks);
+    cfg.blockDim = dim3(kBwdThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((err = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tdq, a)) != cudaSuccess) return err;
     const long long n4 = (long long)a.B * a.N * a.Hq * D / 4;
-    dq_convert_kernel<T><<<dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, stream>>>(a, n4);
-    return cudaGetLastError();
+    const long long nb2 = (n4 + 255) / 256;
+    if (nb2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3((unsigned)nb2);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, dq_convert_kernel<T>, a, n4);
 }
 
 }  // namespace
