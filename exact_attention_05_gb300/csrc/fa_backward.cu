@@ -57,6 +57,21 @@
 namespace fa {
 namespace {
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it on the stream has
+// finished.  grid_dep_wait() blocks the calling thread until that kernel has
+// completed and its memory is visible (a no-op for a normal launch);
+// grid_dep_launch_dependents() lets the next such kernel start once every CTA
+// of this grid has called it or exited.
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+
 template <int D>
 struct BwdCfg {
     static constexpr int BM = 128;                        // query rows per Q tile

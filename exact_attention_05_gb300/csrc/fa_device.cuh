@@ -252,20 +252,6 @@ __device__ __forceinline__ void tma_store_wait_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialization may start before the kernel ahead of it on the stream has
-// finished.  grid_dep_wait() blocks the calling thread until that kernel has
-// completed and its memory is visible (a no-op for a normal launch);
-// grid_dep_launch_dependents() lets the next such kernel start once every CTA
-// of this grid has called it or exited.
-__device__ __forceinline__ void grid_dep_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void grid_dep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of the same memory.
 __device__ __forceinline__ void fence_async_shared() {
