@@ -35,6 +35,11 @@
 //     one thread execute in issue order, and PVi(j) is issued first.
 //   * K/V/Q tiles are 128-byte-swizzled 64-column halves written by TMA and
 //     read by the MMA through shared-memory descriptors.
+//   * few tcgen05.commit operations, each at the end of a group of MMAs: a
+//     commit between two MMAs holds the tensor core until the MMAs before it
+//     are done.  S_i(j) is signalled after QK_i(j); since it also covers the
+//     earlier PV_i(j-1) of the same issuing thread, O-done is signalled only
+//     after a tile's last PV, and ring slots are released after the group.
 //   * every wait is bounded; on expiry the CTA records the timeout, drains
 //     its own copies and MMAs, frees TMEM and returns.
 
@@ -225,8 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar(C::B_SFULL + i));
             };
-            // O_i (+)= P_i V from the V tile in ring slot vs
-            auto pv = [&](int i, int vs, bool accumulate) {
+            // O_i (+)= P_i V from the V tile in ring slot vs.  Only the tile's last
+            // PV signals O-done: otherwise the tile's next QK follows, and the
+            // commit of its S (which covers every earlier MMA of this thread) tells
+            // the softmax that O holds every product so far.
+            auto pv = [&](int i, int vs, bool accumulate, bool last) {
                 const uint64_t db = dv0 + uint64_t(vs) * kSlotStep;
                 const uint32_t d_tmem = tmem + C::tm_o(i);
                 const uint32_t a_tmem = tmem + C::tm_p(i);
@@ -239,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ts(d_tmem, a_tmem + kk * 8, db + uint64_t(kk * 16 * 128 >> 4), idesc_pv,
                            (accumulate || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(C::B_ODONE + i));
+                if (last) mma_commit(bar(C::B_ODONE + i));
             };
             auto wait_slot = [&](int slot, uint32_t phase) -> bool {
                 return mbar_wait_spin(bar_full0 + 8u * slot, phase, wc, FA_SITE_MMA_KV);
@@ -289,11 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     have_vk = true;
-                    pv(0, vs, j > 0);
-                    if (!t1) release(vs);
-                    if (j + 1 < nt0) {
-                        qk(0, nks);
-                        if (!t1) release(nks);
+                    pv(0, vs, j > 0, j + 1 >= nt0);
+                    if (j + 1 < nt0) qk(0, nks);
+                    // slot releases after the group (a commit between two MMAs
+                    // holds the tensor core until the MMAs before it are done)
+                    if (!t1) {
+                        release(vs);
+                        if (j + 1 < nt0) release(nks);
                     }
                 }
                 if (t1) {
@@ -303,12 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    pv(1, vs, j > 0);
+                    pv(1, vs, j > 0, !next_k);
+                    if (next_k) qk(1, nks);
                     release(vs);
-                    if (next_k) {
-                        qk(1, nks);
-                        release(nks);
-                    }
+                    if (next_k) release(nks);
                 }
                 ks = nks;
                 kph = nkph;
@@ -380,14 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rescale = true;
             }
             if (__any_sync(0xffffffffu, rescale)) {
-                // O must hold every PV product so far before it is scaled: PV(j-1)
-                // was issued before QK(j), whose completion we just waited for.
-                got = mbar_wait(bar(C::B_ODONE + tile), (j - 1) & 1, wc, FA_SITE_SOFTMAX_O);
-                if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                // O holds every PV product so far: PV(j-1) was issued before QK(j)
+                // by the same thread, and the commit of S(j), which we waited for,
+                // signals once every MMA issued before it is done.
                 const uint32_t o_addr = lane_base + C::tm_o(tile);
 #pragma unroll 1
                 for (int c = 0; c < D / 16; ++c) {
@@ -434,10 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ------------------------------------------------------------ epilogue
         if (ok) {
-            // PV(nti-2) completed before QK(nti-1) did, so the barrier is at the
-            // phase of PV(nti-1) now.
-            const bool got =
-                mbar_wait(bar(C::B_ODONE + tile), (nti - 1) & 1, wc, FA_SITE_SOFTMAX_O);
+            // the tile's last PV is the only one that signals O-done
+            const bool got = mbar_wait(bar(C::B_ODONE + tile), 0, wc, FA_SITE_SOFTMAX_O);
             ok = __all_sync(0xffffffffu, got);
         }
         uint8_t* stage = smem + C::Q_OFF + tile * C::TILE_BYTES;  // Q_i is dead by now
