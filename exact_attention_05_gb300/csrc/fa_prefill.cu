@@ -22,7 +22,8 @@
 //                  the epilogue (O / l -> smem -> TMA store, LSE -> global);
 //                  each warp signals its P with one arrive (after __syncwarp);
 //       warp 8     TMA producer: Q0, Q1 once, then K0, V0, K1, V1, ... into a
-//                  ring of shared-memory slots;
+//                  ring of shared-memory slots, reusing a slot once the S
+//                  signal that covers its last reader has fired;
 //       warp 9     TMEM allocator and single-thread tcgen05 MMA issuer.
 //   * the tensor core ping-pongs between the tiles:
 //       ... PV0(j)  QK0(j+1)  PV1(j)  QK1(j+1)  PV0(j+1) ...
@@ -37,9 +38,11 @@
 //     read by the MMA through shared-memory descriptors.
 //   * few tcgen05.commit operations, each at the end of a group of MMAs: a
 //     commit between two MMAs holds the tensor core until the MMAs before it
-//     are done.  S_i(j) is signalled after QK_i(j); since it also covers the
-//     earlier PV_i(j-1) of the same issuing thread, O-done is signalled only
-//     after a tile's last PV, and ring slots are released after the group.
+//     are done.  S_i(j) is signalled after QK_i(j); since it also covers every
+//     earlier MMA of the single issuing thread, O-done is signalled only after
+//     a tile's last PV, and ring slots need no signal of their own: the
+//     producer reuses the slot of K_m once the last tile's S(m) is signalled,
+//     and that of V_m once its S(m+1) is (QK(m+1) follows PV(m)).
 //   * every wait is bounded; on expiry the CTA records the timeout, drains
 //     its own copies and MMAs, frees TMEM and returns.
 
@@ -67,13 +70,12 @@ struct PrefillCfg {
     // barrier indices
     static constexpr int B_QFULL = 0;
     static constexpr int B_FULL = 1;                       // NSLOT of them
-    static constexpr int B_EMPTY = 1 + NSLOT;              // NSLOT of them
-    static constexpr int B_SFULL = 1 + 2 * NSLOT;          // one per Q tile
-    static constexpr int B_PFULL = 3 + 2 * NSLOT;          // one per Q tile
-    static constexpr int B_ODONE = 5 + 2 * NSLOT;          // one per Q tile
-    static constexpr int B_DRAIN = 7 + 2 * NSLOT;
-    static constexpr int B_QFULL1 = 8 + 2 * NSLOT;         // Q1 (B_QFULL covers Q0)
-    static constexpr int NBAR = 9 + 2 * NSLOT;
+    static constexpr int B_SFULL = 1 + NSLOT;              // one per Q tile (also frees ring slots)
+    static constexpr int B_PFULL = 3 + NSLOT;              // one per Q tile
+    static constexpr int B_ODONE = 5 + NSLOT;              // one per Q tile
+    static constexpr int B_DRAIN = 7 + NSLOT;
+    static constexpr int B_QFULL1 = 8 + NSLOT;             // Q1 (B_QFULL covers Q0)
+    static constexpr int NBAR = 9 + NSLOT;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
     // TMEM columns
@@ -128,10 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_QFULL1), 1);
-        for (int i = 0; i < C::NSLOT; ++i) {
-            mbar_init(bar(C::B_FULL + i), 1);
-            mbar_init(bar(C::B_EMPTY + i), 1);
-        }
+        for (int i = 0; i < C::NSLOT; ++i) mbar_init(bar(C::B_FULL + i), 1);
         for (int i = 0; i < C::NQ; ++i) {
             mbar_init(bar(C::B_SFULL + i), 1);
             mbar_init(bar(C::B_PFULL + i), 4);  // one arrive per softmax warp
@@ -178,10 +177,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q1_issued = true;
                 }
                 const int slot = L % C::NSLOT;
-                const uint32_t parity = ((L / C::NSLOT) & 1) ^ 1;
-                if (!mbar_wait(bar(C::B_EMPTY + slot), parity, wc, FA_SITE_PRODUCER_SLOT)) {
-                    ok = false;
-                    break;
+                if (L >= C::NSLOT) {
+                    // The slot's previous load must be consumed.  Its last reader is
+                    // the last tile's QK(m) for K_m, or its PV(m) for V_m, which
+                    // that tile's QK(m+1) follows; the commit of that QK's S covers
+                    // every MMA issued before it.  (The MMA issuer cannot get two
+                    // S phases ahead of this wait: it needs the loads that follow.)
+                    const int prev = L - C::NSLOT;
+                    const int phase = (prev >> 1) + (prev & 1);
+                    if (!mbar_wait(bar(C::B_SFULL + (t1 ? 1 : 0)), uint32_t(phase) & 1u, wc,
+                                   FA_SITE_PRODUCER_SLOT)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE_BYTES);
                 const uint32_t dst = sbase + C::SLOT_OFF + slot * C::TILE_BYTES;
@@ -215,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dq1 = dq0 + kSlotStep;
             const uint64_t dk0 = smem_desc(sbase + C::SLOT_OFF, 16, 1024);         // K-major view
             const uint64_t dv0 = smem_desc(sbase + C::SLOT_OFF, C::SUB_BYTES, 1024); // MN-major view
-            const uint32_t bar_full0 = bar(C::B_FULL), bar_empty0 = bar(C::B_EMPTY);
+            const uint32_t bar_full0 = bar(C::B_FULL);
             // S_i = Q_i K^T from the K tile in ring slot ks
             auto qk = [&](int i, int ks) {
                 const uint64_t da = i ? dq1 : dq0;
@@ -252,7 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto wait_slot = [&](int slot, uint32_t phase) -> bool {
                 return mbar_wait_spin(bar_full0 + 8u * slot, phase, wc, FA_SITE_MMA_KV);
             };
-            auto release = [&](int slot) { mma_commit(bar_empty0 + 8u * slot); };
 
             // ring positions of K_j (load 2j) and V_j (load 2j+1)
             int ks = 0, vs = 1 % C::NSLOT;
@@ -276,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         qk(1, ks);
                     }
                 }
-                release(ks);  // K0
             }
             // Everything a tile's group of MMAs needs (its P, V_j and the next K
             // tile) is waited for before the group is issued, so that PV_i(j) and
@@ -299,12 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     have_vk = true;
                     pv(0, vs, j > 0, j + 1 >= nt0);
                     if (j + 1 < nt0) qk(0, nks);
-                    // slot releases after the group (a commit between two MMAs
-                    // holds the tensor core until the MMAs before it are done)
-                    if (!t1) {
-                        release(vs);
-                        if (j + 1 < nt0) release(nks);
-                    }
                 }
                 if (t1) {
                     if ((!have_vk && (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph)))) ||
@@ -315,8 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     pv(1, vs, j > 0, !next_k);
                     if (next_k) qk(1, nks);
-                    release(vs);
-                    if (next_k) release(nks);
                 }
                 ks = nks;
                 kph = nkph;
