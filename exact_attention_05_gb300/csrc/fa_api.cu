@@ -335,17 +335,15 @@ FA_EXPORT fa_status fa_decode_fused(const void* q, const void* k, const void* v,
     if (chunk <= 0) return FA_ERR_INVALID_ARG;
     const long long nc = ((long long)M + chunk - 1) / chunk;
     if (nc * B * Hkv > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-    const int ngroups = (int)((nc + fa::kDecodeMergeGroup - 1) / fa::kDecodeMergeGroup);
     DeviceState* st = nullptr;
     if ((s = device_state(&st)) != FA_OK) return s;
+    // chunk partials, then the stripe partials (at most one stripe per chunk)
     const size_t part_elems = (size_t)B * Hq * nc * d;
-    const size_t grp_elems = (size_t)B * Hq * ngroups * d;
-    const size_t floats = part_elems + (size_t)B * Hq * nc + grp_elems + (size_t)B * Hq * ngroups;
+    const size_t floats = 2 * (part_elems + (size_t)B * Hq * nc);
     void* ws = nullptr;
     if ((s = workspace(st, (cudaStream_t)stream, floats * sizeof(float), &ws)) != FA_OK) return s;
     int* tk_counts = nullptr;
-    if ((s = tickets(st, (cudaStream_t)stream, (size_t)B * Hkv * (ngroups + 1), &tk_counts)) != FA_OK)
-        return s;
+    if ((s = tickets(st, (cudaStream_t)stream, (size_t)B * Hkv, &tk_counts)) != FA_OK) return s;
     CUtensorMap tk, tv;
     if (!fa::encode_decode_maps(g_encode, k, v, dtype, d, Hkv, M, B, &tk, &tv)) return FA_ERR_CUDA;
     fa::DecodeArgs a{};
@@ -356,9 +354,8 @@ FA_EXPORT fa_status fa_decode_fused(const void* q, const void* k, const void* v,
     a.o_part = f;
     a.lse_part = f + part_elems;
     a.g_o = a.lse_part + (size_t)B * Hq * nc;
-    a.g_lse = a.g_o + grp_elems;
+    a.g_lse = a.g_o + part_elems;
     a.tickets = tk_counts;
-    a.ngroups = ngroups;
     a.B = B;
     a.Hq = Hq;
     a.Hkv = Hkv;

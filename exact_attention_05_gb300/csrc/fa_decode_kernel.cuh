@@ -136,17 +136,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     return r;
 }
 
-// Merges n partial results (fp32 rows of D at rows + i*D, normalised, with
-// log2-domain LSEs lse[i]) into one with the LSE weights of the page's Step 2:
+// Merges n partial results (fp32 rows of D at rows + i*stride*D, normalised,
+// with log2-domain LSEs lse[i*stride]) into one with the LSE weights of the page's Step 2:
 // w_i = 2^(lse_i - glse), glse = log2 sum_i 2^lse_i.  128 threads; thread t < D
 // owns column t.  Returns glse; writes the row to out_f (fp32) or out_t.  If
 // every partial is empty (lse = -inf) the row is zero and glse is -inf.
 template <int D, typename T>
-__device__ float merge_partials(const float* lse, const float* rows, int n, float* red,
+__device__ float merge_partials(const float* lse, const float* rows, int n, int stride, float* red,
                                 float* out_f, T* out_t) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float mx = -INFINITY;
-    for (int i = tid; i < n; i += 128) mx = fmaxf(mx, __ldcg(lse + i));
+    for (int i = tid; i < n; i += 128) mx = fmaxf(mx, __ldcg(lse + size_t(i) * stride));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if (lane == 0) red[warp] = mx;
@@ -155,7 +155,7 @@ __device__ float merge_partials(const float* lse, const float* rows, int n, floa
     __syncthreads();
     const float ref = mx == -INFINITY ? 0.f : mx;
     float sm = 0.f;
-    for (int i = tid; i < n; i += 128) sm += fast_exp2(__ldcg(lse + i) - ref);
+    for (int i = tid; i < n; i += 128) sm += fast_exp2(__ldcg(lse + size_t(i) * stride) - ref);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
     if (lane == 0) red[warp] = sm;
@@ -168,8 +168,8 @@ __device__ float merge_partials(const float* lse, const float* rows, int n, floa
         if (mx != -INFINITY) {
 #pragma unroll 8
             for (int i = 0; i < n; ++i)
-                acc = fmaf(fast_exp2(__ldcg(lse + i) - glse), __ldcg(rows + size_t(i) * D + tid),
-                           acc);
+                acc = fmaf(fast_exp2(__ldcg(lse + size_t(i) * stride) - glse),
+                           __ldcg(rows + size_t(i) * stride * D + tid), acc);
         }
         if (out_f != nullptr) out_f[tid] = acc;
         if (out_t != nullptr) out_t[tid] = static_cast<T>(acc);
@@ -177,58 +177,48 @@ __device__ float merge_partials(const float* lse, const float* rows, int n, floa
     return glse;
 }
 
-// Single launch (no merge kernel): the last CTA to finish a group of
-// kDecodeMergeGroup chunks merges the group's partials; the last group merge of
-// a (b, kv head) merges the group results into O and LSE.  Tickets are reset by
-// whoever finishes them, so they are zero again when the kernel ends.
+// Single launch (no merge kernel).  The persistent stripes write their chunks'
+// partials as in the two-kernel path; then every stripe CTA merges its own
+// chunks (rows stride nstripes apart, still in L2) into one stripe partial, and
+// the last stripe CTA of a (b, kv head) to finish merges the stripe partials
+// into O and LSE.  The ticket is reset by whoever finishes it, so it is zero
+// again when the kernel ends.
 template <int D, typename T>
-__device__ void fused_merge_tail(const DecodeArgs& a, bool ok, int b, int kvh, int c) {
+__device__ void fused_stripe_tail(const DecodeArgs& a, bool ok, int b, int kvh, int stripe) {
     __shared__ int s_last;
     __shared__ float s_red[4];
     const int tid = threadIdx.x;
     const int g = a.Hq / a.Hkv;
-    // The barrier orders every thread's partial stores before thread 0's
-    // device-scope fence, which is cumulative; then the ticket.
+    // The barrier orders every thread's partial stores before the merge reads
+    // them back (and, through thread 0's cumulative fence, before the ticket).
     if (!__syncthreads_and(ok)) return;
-    const int grp = c / kDecodeMergeGroup;
-    const int c0 = grp * kDecodeMergeGroup;
-    const int gsize = min(kDecodeMergeGroup, a.nc - c0);
-    int* t1 = a.tickets + (size_t(b) * a.Hkv + kvh) * a.ngroups + grp;
-    int* t2 = a.tickets + size_t(a.B) * a.Hkv * a.ngroups + (size_t(b) * a.Hkv + kvh);
-    if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(t1, 1) == gsize - 1;
-        if (s_last) __threadfence();  // acquire: the others' partials are visible
-    }
-    __syncthreads();
-    if (!s_last) return;
+    const int nmine = (a.nc - stripe + a.nstripes - 1) / a.nstripes;  // chunks stripe, stripe + nstripes, ...
     for (int gi = 0; gi < g; ++gi) {
         const size_t bh = size_t(b) * a.Hq + kvh * g + gi;
-        const size_t src = bh * a.nc + c0;
-        const size_t dst = bh * a.ngroups + grp;
-        const float glse = merge_partials<D, T>(a.lse_part + src, a.o_part + src * D, gsize, s_red,
-                                                a.g_o + dst * D, nullptr);
+        const size_t src = bh * a.nc + stripe;
+        const size_t dst = bh * a.nstripes + stripe;
+        const float glse = merge_partials<D, T>(a.lse_part + src, a.o_part + src * D, nmine,
+                                                a.nstripes, s_red, a.g_o + dst * D, nullptr);
         if (tid == 0) a.g_lse[dst] = glse;
         __syncthreads();
     }
-    __syncthreads();
+    int* t = a.tickets + (size_t(b) * a.Hkv + kvh);
     if (tid == 0) {
-        *t1 = 0;
         __threadfence();
-        s_last = atomicAdd(t2, 1) == a.ngroups - 1;
-        if (s_last) __threadfence();
+        s_last = atomicAdd(t, 1) == a.nstripes - 1;
+        if (s_last) __threadfence();  // acquire: the other stripes' partials are visible
     }
     __syncthreads();
     if (!s_last) return;
     for (int gi = 0; gi < g; ++gi) {
         const size_t bh = size_t(b) * a.Hq + kvh * g + gi;
-        const float glse = merge_partials<D, T>(a.g_lse + bh * a.ngroups, a.g_o + bh * a.ngroups * D,
-                                                a.ngroups, s_red, nullptr,
+        const float glse = merge_partials<D, T>(a.g_lse + bh * a.nstripes, a.g_o + bh * a.nstripes * D,
+                                                a.nstripes, 1, s_red, nullptr,
                                                 reinterpret_cast<T*>(a.o) + bh * D);
         if (tid == 0 && a.lse != nullptr) a.lse[bh] = glse * kLn2;
         __syncthreads();
     }
-    if (tid == 0) *t2 = 0;
+    if (tid == 0) *t = 0;
 }
 
 // The merge kernel.  One CTA of 128 threads per (b, h) and 16 output columns:
@@ -727,7 +717,6 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
             }
             __syncthreads();
         }
-        if constexpr (FUSED) fused_merge_tail<D, T>(a, ok, b, kvh, c);
     }
     // every issued copy must have landed before the CTA exits (only a wait that
     // gave up leaves any outstanding)
@@ -736,7 +725,9 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
             mbar_drain_wait(bar0 + 8 * (n % C::NSLOT), uint32_t(n / C::NSLOT) & 1u, wc,
                             FA_SITE_DRAIN);
     }
-    if constexpr (!FUSED) {
+    if constexpr (FUSED) {
+        fused_stripe_tail<D, T>(a, ok, b, kvh, stripe);
+    } else {
         // this CTA's partials are written: the merge grid may be scheduled
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
@@ -808,9 +799,6 @@ cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     const long long nbh = (long long)a.B * a.Hkv;
     long long nstripes = (long long)occ * sms / nbh;
     nstripes = nstripes < 1 ? 1 : (nstripes > a.nc ? a.nc : nstripes);
-    // the single launch keeps one chunk per CTA: a CTA that merges a group must
-    // not hold up a stream of further chunks behind it
-    if (FUSED) nstripes = a.nc;
     const long long nblocks = nbh * nstripes;
     if (nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     DecodeArgs la = a;

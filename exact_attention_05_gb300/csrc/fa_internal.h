@@ -58,11 +58,11 @@ struct DecodeArgs {
     const int* seq_lens;
     int page;
     int max_pages;
-    // single-launch variant only: group partials and self-resetting tickets
-    float* g_o;            // [B, Hq, ngroups, d] fp32
-    float* g_lse;          // [B, Hq, ngroups] fp32, log2 domain
-    int* tickets;          // B*Hkv*ngroups group tickets, then B*Hkv head tickets; all zero between calls
-    int ngroups;           // ceil(nc / kDecodeMergeGroup)
+    // single-launch variant only: one merged partial per stripe (room for nc
+    // stripes, the most there can be) and a self-resetting ticket per (b, kv head)
+    float* g_o;            // [B, Hq, nstripes, d] fp32
+    float* g_lse;          // [B, Hq, nstripes] fp32, log2 domain
+    int* tickets;          // [B, Hkv]; all zero between calls
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -130,6 +130,5 @@ cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cud
 // Geometry the host needs to build tensor maps.
 constexpr int kPrefillTile = 128;   // query rows per tile and keys per KV tile
 constexpr int kDecodeSubTile = 128; // keys per decode sub-tile
-constexpr int kDecodeMergeGroup = 32;  // chunks merged together at the first level (single launch)
 
 }  // namespace fa

@@ -112,15 +112,16 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
 /*
  * Split-KV decode in a single launch.  Same arguments, layouts, results and
  * errors as fa_decode; the chunk partials are merged by the chunk kernel
- * itself instead of a second kernel: the last CTA to finish each group of 32
- * consecutive chunks of a (b, kv head) merges that group's partials with the
- * LSE weights of "CUDA 实现 Flash Decoding" section 2.2 Step 2, and the last
- * group to finish merges the group results into o and lse (the merge is
- * associative, so the result is the same up to rounding order).  The
- * page's section 8 lists this single launch as its fourth lever.
+ * itself instead of a second kernel.  Each persistent CTA walks the chunks
+ * s, s + S, s + 2S, ... of one (b, kv head) (S CTAs per (b, kv head), as many
+ * as fit in one wave); once its chunks are done it merges their partials with
+ * the LSE weights of "CUDA 实现 Flash Decoding" section 2.2 Step 2, and the last
+ * of the S CTAs to finish merges the S results into o and lse (the merge is
+ * associative, so the result is the same up to rounding order).  The page's
+ * section 8 lists this single launch as its fourth lever.
  *
- * Workspace: the same per-(device, stream) buffer as fa_decode, plus the group
- * results (B*Hq*ceil(nc/32)*(d+1) fp32), plus B*Hkv*(ceil(nc/32)+1) int
+ * Workspace: the same per-(device, stream) buffer as fa_decode, plus room for
+ * one merged result per CTA (at most B*Hq*nc*(d+1) fp32), plus B*Hkv int
  * tickets that are zeroed when allocated and reset by the kernel itself; after
  * a call that reported FA_ERR_TIMEOUT call fa_release_workspaces() before the
  * next call on that stream.
