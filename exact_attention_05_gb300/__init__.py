@@ -64,6 +64,8 @@ def load_library():
         I, F = ctypes.c_int, ctypes.c_float
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, I, F, I, vp]
         lib.fa_fwd.restype = I
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, I, F, I, vp]
+        lib.fa_fwd_host.restype = I
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, I, I, I, I, I, I, I, F, I, vp]
         lib.fa_bwd.restype = I
         lib.fa_decode.argtypes = [vp, vp, vp, vp, fp, I, I, I, I, I, I, F, I, vp]
@@ -126,6 +128,16 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, M, d, causal, scale, dtype, stream=No
                                int(Hkv), int(N), int(M), int(d), int(causal), float(scale),
                                int(dtype), _stream(stream))
     return _check(st, "fa_fwd") if check else st
+
+
+def fa_fwd_host(q, k, v, o, lse, B, Hq, Hkv, N, M, d, causal, scale, dtype, stream=None,
+                check=True) -> int:
+    """fa_fwd on host (CPU, preferably pinned) tensors, transfers overlapped with
+    the kernels; synchronize `stream` before reading o and lse."""
+    st = load_library().fa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                    int(Hq), int(Hkv), int(N), int(M), int(d), int(causal),
+                                    float(scale), int(dtype), _stream(stream))
+    return _check(st, "fa_fwd_host") if check else st
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, M, d, causal, scale, dtype,
@@ -233,6 +245,26 @@ def attention_forward(q, k, v, causal: bool, scale: float, out=None, lse=None, w
             raise ValueError("tensors must be contiguous")
     fa_fwd(q, k, v, out, lse, B, Hq, Hkv, N, M, d, int(bool(causal)), scale, _dtype_code(q),
            stream)
+    return out, lse
+
+
+def attention_forward_host(q, k, v, causal: bool, scale: float, out=None, lse=None,
+                           with_lse=True, stream=None):
+    """attention_forward on CPU tensors (pin them for the transfers to overlap the
+    kernels): returns pinned CPU O [B,N,Hq,d] and LSE [B,Hq,N], complete once
+    `stream` (default: the current CUDA stream) is synchronized."""
+    import torch
+    B, N, Hq, d = q.shape
+    _, M, Hkv, _ = k.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=True)
+    for t in (q, k, v, out):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CPU tensors")
+    fa_fwd_host(q, k, v, out, lse, B, Hq, Hkv, N, M, d, int(bool(causal)), scale, _dtype_code(q),
+                stream)
     return out, lse
 
 

@@ -30,11 +30,24 @@ struct Workspace {
     size_t nticket = 0;
 };
 
+// Copy streams and events of fa_fwd_host for one caller stream: chunk c's
+// inputs go in on `in` while chunk c-1 computes on the caller's stream and chunk
+// c-2's outputs come back on `out`; slot c % 2 of the device staging is reused
+// once chunk c-2's outputs are copied out.
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t landed[2] = {nullptr, nullptr}, computed[2] = {nullptr, nullptr},
+                copied[2] = {nullptr, nullptr};
+    bool ready = false;
+};
+
 struct DeviceState {
     bool checked = false;
     bool supported = false;
     int* status = nullptr;
     std::map<cudaStream_t, Workspace> workspaces;
+    std::map<cudaStream_t, HostPipe> pipes;
 };
 
 std::mutex g_mu;
@@ -226,6 +239,111 @@ FA_EXPORT fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
     a.status = st->status;
     a.timeout_ns = g_timeout_ns.load();
     return from_cuda(fa::launch_prefill(tq, tk, tv, to, a, d, (int)dtype, (cudaStream_t)stream));
+}
+
+namespace {
+
+// The copy streams and events of fa_fwd_host for (current device, stream).
+fa_status host_pipe(DeviceState* st, cudaStream_t stream, HostPipe** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    HostPipe& p = st->pipes[stream];
+    if (!p.ready) {
+        if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) != cudaSuccess)
+            return FA_ERR_CUDA;
+        for (int i = 0; i < 2; ++i)
+            if (cudaEventCreateWithFlags(&p.landed[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&p.computed[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&p.copied[i], cudaEventDisableTiming) != cudaSuccess)
+                return FA_ERR_CUDA;
+        p.ready = true;
+    }
+    *out = &p;
+    return FA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+FA_EXPORT fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int Hq, int Hkv, int N, int M, int d, int causal,
+                                float scale, fa_dtype dtype, fa_stream_t stream) {
+    fa_status s = check_args(q, k, v, o, lse, B, Hq, Hkv, N, M, d, scale, (int)dtype);
+    if (s != FA_OK) return s;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != FA_OK) return s;
+    const cudaStream_t cs = (cudaStream_t)stream;
+    HostPipe* p = nullptr;
+    if ((s = host_pipe(st, cs, &p)) != FA_OK) return s;
+    // Chunks of (b, group of kv heads with their query heads): one per batch entry
+    // when B >= 4, else about four in all, so that each launch still fills the GPU
+    // with CTAs while the copies of its neighbours run.
+    const int g = Hq / Hkv;
+    int per_b = B >= 4 ? 1 : (4 + B - 1) / B;
+    if (per_b > Hkv) per_b = Hkv;
+    const int hk_max = (Hkv + per_b - 1) / per_b;
+    const int hq_max = hk_max * g;
+    const size_t esz = 2;
+    const size_t row_q = (size_t)Hq * d * esz, row_kv = (size_t)Hkv * d * esz;
+    // device staging, two slots: q, o [N, hq, d]; k, v [M, hk, d]; lse [hq, N]
+    const size_t bq = round256((size_t)N * hq_max * d * esz);
+    const size_t bkv = round256((size_t)M * hk_max * d * esz);
+    const size_t bl = round256((size_t)hq_max * N * sizeof(float));
+    const size_t slot_bytes = 2 * bq + 2 * bkv + bl;
+    void* ws = nullptr;
+    if ((s = workspace(st, cs, 2 * slot_bytes, &ws)) != FA_OK) return s;
+    auto err = [](cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; };
+    if ((s = err(cudaEventRecord(p->start, cs))) != FA_OK) return s;
+    if ((s = err(cudaStreamWaitEvent(p->in, p->start, 0))) != FA_OK) return s;
+    if ((s = err(cudaStreamWaitEvent(p->out, p->start, 0))) != FA_OK) return s;
+    int c = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int kv0 = 0; kv0 < Hkv; kv0 += hk_max, ++c) {
+            const int hk = Hkv - kv0 < hk_max ? Hkv - kv0 : hk_max;
+            const int hq0 = kv0 * g, hq = hk * g;
+            const int slot = c & 1;
+            uint8_t* base = static_cast<uint8_t*>(ws) + slot * slot_bytes;
+            uint8_t* qd = base;
+            uint8_t* od = qd + bq;
+            uint8_t* kd = od + bq;
+            uint8_t* vd = kd + bkv;
+            float* ld = reinterpret_cast<float*>(vd + bkv);
+            // the slot's previous chunk must be copied out (it was computed before that)
+            if (c >= 2 && (s = err(cudaStreamWaitEvent(p->in, p->copied[slot], 0))) != FA_OK)
+                return s;
+            const uint8_t* qh = static_cast<const uint8_t*>(q) + ((size_t)b * N * Hq + hq0) * d * esz;
+            const uint8_t* kh = static_cast<const uint8_t*>(k) + ((size_t)b * M * Hkv + kv0) * d * esz;
+            const uint8_t* vh = static_cast<const uint8_t*>(v) + ((size_t)b * M * Hkv + kv0) * d * esz;
+            const size_t wq = (size_t)hq * d * esz, wkv = (size_t)hk * d * esz;
+            if ((s = err(cudaMemcpy2DAsync(qd, wq, qh, row_q, wq, N, cudaMemcpyHostToDevice, p->in))) != FA_OK ||
+                (s = err(cudaMemcpy2DAsync(kd, wkv, kh, row_kv, wkv, M, cudaMemcpyHostToDevice, p->in))) != FA_OK ||
+                (s = err(cudaMemcpy2DAsync(vd, wkv, vh, row_kv, wkv, M, cudaMemcpyHostToDevice, p->in))) != FA_OK ||
+                (s = err(cudaEventRecord(p->landed[slot], p->in))) != FA_OK ||
+                (s = err(cudaStreamWaitEvent(cs, p->landed[slot], 0))) != FA_OK)
+                return s;
+            if ((s = fa_fwd(qd, kd, vd, od, lse ? ld : nullptr, 1, hq, hk, N, M, d, causal, scale,
+                            dtype, stream)) != FA_OK)
+                return s;
+            if ((s = err(cudaEventRecord(p->computed[slot], cs))) != FA_OK ||
+                (s = err(cudaStreamWaitEvent(p->out, p->computed[slot], 0))) != FA_OK)
+                return s;
+            uint8_t* oh = static_cast<uint8_t*>(o) + ((size_t)b * N * Hq + hq0) * d * esz;
+            if ((s = err(cudaMemcpy2DAsync(oh, row_q, od, wq, wq, N, cudaMemcpyDeviceToHost, p->out))) != FA_OK)
+                return s;
+            if (lse && (s = err(cudaMemcpyAsync(lse + ((size_t)b * Hq + hq0) * N, ld,
+                                                (size_t)hq * N * sizeof(float), cudaMemcpyDeviceToHost,
+                                                p->out))) != FA_OK)
+                return s;
+            if ((s = err(cudaEventRecord(p->copied[slot], p->out))) != FA_OK) return s;
+        }
+    }
+    // the caller's stream is ordered after every copy out
+    for (int i = 0; i < 2 && i < c; ++i)
+        if ((s = err(cudaStreamWaitEvent(cs, p->copied[i], 0))) != FA_OK) return s;
+    return FA_OK;
 }
 
 FA_EXPORT fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -471,7 +589,7 @@ FA_EXPORT void fa_release_workspaces(void) {
     int cur = 0;
     const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
     for (auto& kv : g_devices) {
-        if (kv.second.workspaces.empty()) continue;
+        if (kv.second.workspaces.empty() && kv.second.pipes.empty()) continue;
         if (cudaSetDevice(kv.first) != cudaSuccess) continue;
         cudaDeviceSynchronize();
         for (auto& w : kv.second.workspaces) {
@@ -479,6 +597,19 @@ FA_EXPORT void fa_release_workspaces(void) {
             if (w.second.tickets) cudaFree(w.second.tickets);
         }
         kv.second.workspaces.clear();
+        for (auto& pp : kv.second.pipes) {
+            HostPipe& hp = pp.second;
+            if (!hp.ready) continue;
+            cudaStreamDestroy(hp.in);
+            cudaStreamDestroy(hp.out);
+            cudaEventDestroy(hp.start);
+            for (int i = 0; i < 2; ++i) {
+                cudaEventDestroy(hp.landed[i]);
+                cudaEventDestroy(hp.computed[i]);
+                cudaEventDestroy(hp.copied[i]);
+            }
+        }
+        kv.second.pipes.clear();
     }
     if (have_cur) cudaSetDevice(cur);
 }

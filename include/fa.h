@@ -87,6 +87,31 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  float scale, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * fa_fwd on host-resident tensors: the same operation, arguments, layouts and
+ * results, with q, k, v, o and lse in host memory.  The problem is cut into
+ * independent chunks of (b, a group of kv heads with their query heads), about
+ * four in all (one per batch entry when B >= 4).  Chunk c's inputs are copied to
+ * the device on an internal stream while chunk c-1 runs fa_fwd on `stream` and
+ * chunk c-2's o and lse are copied back on another internal stream, so the
+ * transfers overlap the kernels.  Each chunk gives exactly what fa_fwd gives for
+ * those heads.
+ *
+ * Host memory should be page-locked (pinned) for the copies to overlap;
+ * pageable memory works, with copies that do not overlap.  Returns FA_OK once
+ * the work is enqueued; `stream` is ordered after the last copy back, so
+ * synchronize it before reading o and lse, and keep the inputs unchanged until
+ * then.  Calls on one stream must come from one host thread at a time.
+ *
+ * Workspace: two chunks' device staging per (device, stream), from the same
+ * cached buffer as fa_decode; two internal streams and a few events per
+ * (device, stream), released by fa_release_workspaces().
+ * Errors: as fa_fwd.
+ */
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int Hq, int Hkv, int N, int M, int d, int causal,
+                      float scale, fa_dtype dtype, fa_stream_t stream);
+
+/*
  * Split-KV flash decoding (one query row per head).
  *
  *   q   [B, 1, Hq, d]   fp16/bf16, device

@@ -52,6 +52,15 @@ def fwd(**kw):
                      args["scale"], args["dtype"], stream=0, check=False)
 
 
+def fwd_host(**kw):
+    args = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=None, B=1, Hq=2, Hkv=2, N=128, M=128, d=128,
+                causal=0, scale=0.1, dtype=0)
+    args.update(kw)
+    return fa.fa_fwd_host(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                          args["Hq"], args["Hkv"], args["N"], args["M"], args["d"], args["causal"],
+                          args["scale"], args["dtype"], stream=0, check=False)
+
+
 def dec(**kw):
     args = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=None, B=1, Hq=2, Hkv=2, M=128, d=128,
                 chunk=128, scale=0.1, dtype=0)
@@ -90,7 +99,7 @@ def decp(**kw):
                               args["chunk"], args["scale"], args["dtype"], stream=0, check=False)
 
 
-@pytest.mark.parametrize("call", [fwd, dec, dec8, decp, bwd])
+@pytest.mark.parametrize("call", [fwd, fwd_host, dec, dec8, decp, bwd])
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), fa.FA_ERR_INVALID_ARG),
     (dict(k=None), fa.FA_ERR_INVALID_ARG),
@@ -126,6 +135,7 @@ def test_invalid_arguments(lib, call, kw, code):
 @pytest.mark.parametrize("kw", [dict(N=0), dict(N=-1), dict(causal=2), dict(causal=-1)])
 def test_invalid_forward_only_arguments(lib, kw):
     assert fwd(**kw) == fa.FA_ERR_INVALID_ARG
+    assert fwd_host(**kw) == fa.FA_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("kw", [dict(chunk=0), dict(chunk=-128),
