@@ -111,15 +111,25 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank lines (string literals in these
+    files hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_digest(kernel: str) -> str:
-    """Short hash of the source files a kernel is compiled from."""
+    """Short hash of the code (comments left out) of the files a kernel is
+    compiled from: an edit to a comment does not void a recorded capture."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_05_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

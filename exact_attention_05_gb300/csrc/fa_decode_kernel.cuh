@@ -13,15 +13,19 @@
 // are kept in base 2 (scale * log2 e folded in), which changes no result.
 //
 // Layout of the work on GB300:
-//   * one CTA (128 threads) per (b, kv head, chunk) serves every query head of
-//     the GQA group, so each K/V byte is read from HBM once; the block index is
-//     ordered with (b, kv head) fastest so that CTAs running together read
-//     whole contiguous key rows.  One thread issues TMA copies of the chunk's
-//     K and V sub-tiles (128 keys) at CTA start; V streams in while the scores
-//     are computed.
+//   * persistent CTAs of 128 threads, nstripes per (b, kv head) (one wave):
+//     the CTA with stripe s walks chunks s, s + nstripes, ... and serves every
+//     query head of the GQA group, so each K/V byte is read from HBM once; the
+//     block index is ordered with (b, kv head) fastest so that CTAs running
+//     together read whole contiguous key rows.  Warp 0 streams the K and V
+//     sub-tiles (128 keys) through a ring of TMA slots in the order the chunks
+//     consume them.
 //   * scores: thread <-> key, the full dot product read from a swizzled K
-//     tile (one 16-byte chunk per step, conflict-free); softmax per head by
-//     one warp; P.V: thread <-> (column pair, key group).
+//     tile (one 16-byte chunk per step, conflict-free); softmax in registers
+//     with warp-shuffle reductions; P.V: thread <-> (4 columns, key group).
+//   * the merge: a second kernel (one CTA per (b, h) and 16 columns), or, in
+//     the single launch, each stripe CTA merges its own chunks and the last
+//     stripe of a (b, kv head) merges the stripes.
 //   * e4m3 K/V: the same tiles at one byte per element; the per-kv-head scales
 //     are applied once per score (s = k_scale * q.k8) and once per output
 //     (o = v_scale * sum_j p_j v8_j), which is exact algebra.
