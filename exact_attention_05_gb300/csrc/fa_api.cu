@@ -455,9 +455,12 @@ FA_EXPORT fa_status fa_decode_fused(const void* q, const void* k, const void* v,
     if (nc * B * Hkv > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     DeviceState* st = nullptr;
     if ((s = device_state(&st)) != FA_OK) return s;
-    // chunk partials, then the stripe partials (at most one stripe per chunk)
+    // chunk partials, then the stripe partials (at most one stripe per chunk);
+    // the LSE blocks are padded to 64 floats so that every row block starts on
+    // a 256-byte boundary (the kernel stores the rows as float4)
     const size_t part_elems = (size_t)B * Hq * nc * d;
-    const size_t floats = 2 * (part_elems + (size_t)B * Hq * nc);
+    const size_t lse_elems = ((size_t)B * Hq * nc + 63) & ~size_t(63);
+    const size_t floats = 2 * (part_elems + lse_elems);
     void* ws = nullptr;
     if ((s = workspace(st, (cudaStream_t)stream, floats * sizeof(float), &ws)) != FA_OK) return s;
     int* tk_counts = nullptr;
@@ -471,7 +474,7 @@ FA_EXPORT fa_status fa_decode_fused(const void* q, const void* k, const void* v,
     a.lse = lse;
     a.o_part = f;
     a.lse_part = f + part_elems;
-    a.g_o = a.lse_part + (size_t)B * Hq * nc;
+    a.g_o = a.lse_part + lse_elems;
     a.g_lse = a.g_o + part_elems;
     a.tickets = tk_counts;
     a.B = B;

@@ -24,7 +24,8 @@
 //     tile (one 16-byte chunk per step, conflict-free); softmax in registers
 //     with warp-shuffle reductions; P.V: thread <-> (4 columns, key group).
 //   * the merge: a second kernel (one CTA per (b, h) and 16 columns), or, in
-//     the single launch, each stripe CTA merges its own chunks and the last
+//     the single launch, each stripe CTA merges its own chunks (on the fly,
+//     when one pass over a tile serves all its query heads) and the last
 //     stripe of a (b, kv head) merges the stripes.
 //   * e4m3 K/V: the same tiles at one byte per element; the per-kv-head scales
 //     are applied once per score (s = k_scale * q.k8) and once per output
@@ -181,14 +182,16 @@ __device__ float merge_partials(const float* lse, const float* rows, int n, int 
     return glse;
 }
 
-// Single launch (no merge kernel).  The persistent stripes write their chunks'
-// partials as in the two-kernel path; then every stripe CTA merges its own
-// chunks (rows stride nstripes apart, still in L2) into one stripe partial, and
-// the last stripe CTA of a (b, kv head) to finish merges the stripe partials
-// into O and LSE.  The ticket is reset by whoever finishes it, so it is zero
-// again when the kernel ends.
+// Single launch (no merge kernel).  Every stripe CTA leaves one partial per
+// query head: `merged` when the chunk loop already carried its running state
+// across the stripe's chunks (one pass per tile), else it merges the chunk
+// partials it wrote (rows stride nstripes apart, still in L2).  The last stripe
+// CTA of a (b, kv head) to finish then merges the stripe partials into O and
+// LSE.  The ticket is reset by whoever finishes it, so it is zero again when
+// the kernel ends.
 template <int D, typename T>
-__device__ void fused_stripe_tail(const DecodeArgs& a, bool ok, int b, int kvh, int stripe) {
+__device__ void fused_stripe_tail(const DecodeArgs& a, bool ok, int b, int kvh, int stripe,
+                                  bool merged) {
     __shared__ int s_last;
     __shared__ float s_red[4];
     const int tid = threadIdx.x;
@@ -197,7 +200,7 @@ __device__ void fused_stripe_tail(const DecodeArgs& a, bool ok, int b, int kvh, 
     // them back (and, through thread 0's cumulative fence, before the ticket).
     if (!__syncthreads_and(ok)) return;
     const int nmine = (a.nc - stripe + a.nstripes - 1) / a.nstripes;  // chunks stripe, stripe + nstripes, ...
-    for (int gi = 0; gi < g; ++gi) {
+    for (int gi = 0; gi < g && !merged; ++gi) {
         const size_t bh = size_t(b) * a.Hq + kvh * g + gi;
         const size_t src = bh * a.nc + stripe;
         const size_t dst = bh * a.nstripes + stripe;
@@ -460,6 +463,65 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
     const int kq = tid / C::NCG;
     uint16_t* ph = reinterpret_cast<uint16_t*>(smem + C::PH_OFF);
 
+    // running max and sum of each head (kept identically by every thread) and two
+    // accumulators per head (even and odd keys: independent FMA chains)
+    float m_run[GP], l_run[GP], alpha[GP];
+    float4 acc[GP], acc2[GP];
+    auto reset = [&]() {
+#pragma unroll
+        for (int gi = 0; gi < GP; ++gi) {
+            m_run[gi] = -INFINITY;
+            l_run[gi] = 0.f;
+            acc[gi] = acc2[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    // Adds up the key groups' accumulators of heads hg .. hg+GP-1 and writes the
+    // normalised rows and log2-domain LSEs at o_dst + r*D, lse_dst[r], with
+    // r = (b*Hq + h) * per_head + idx.  Collective (all 128 threads).
+    auto write_partial = [&](int hg, float* o_dst, float* lse_dst, int per_head, int idx) {
+        float4* red4 = reinterpret_cast<float4*>(red);
+#pragma unroll
+        for (int gi = 0; gi < GP; ++gi) {
+            acc[gi].x += acc2[gi].x;
+            acc[gi].y += acc2[gi].y;
+            acc[gi].z += acc2[gi].z;
+            acc[gi].w += acc2[gi].w;
+        }
+        if (kq > 0) {
+#pragma unroll
+            for (int gi = 0; gi < GP; ++gi) red4[((kq - 1) * C::GMAX + gi) * C::NCG + cg] = acc[gi];
+        }
+        __syncthreads();
+        if (kq == 0) {
+#pragma unroll
+            for (int gi = 0; gi < GP; ++gi) {
+                float4 t = acc[gi];
+#pragma unroll
+                for (int u = 1; u < C::KQ; ++u) {
+                    const float4 o = red4[((u - 1) * C::GMAX + gi) * C::NCG + cg];
+                    t.x += o.x;
+                    t.y += o.y;
+                    t.z += o.z;
+                    t.w += o.w;
+                }
+                const int h = kvh * g + hg + gi;
+                const size_t r = (size_t(b) * a.Hq + h) * per_head + idx;
+                const float inv = vscale / l_run[gi];
+                reinterpret_cast<float4*>(o_dst + r * D)[cg] =
+                    make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+                if (cg == 0) lse_dst[r] = m_run[gi] + log2f(l_run[gi]);
+            }
+        }
+        __syncthreads();
+    };
+    // Single launch with one pass over each tile (all g heads at once): the
+    // stripe's chunks are merged on the fly.  The running max, sum and
+    // accumulators carry on from one chunk to the next (Step 2's merge, done
+    // online), and only the stripe's own result is written.  Every stripe owns
+    // at least one chunk with keys (nstripes <= nc, contiguous K/V).
+    const bool run_stripe = FUSED && npass == 1;
+    if (run_stripe) reset();
+
     for (int c = stripe; c < a.nc && ok; c += a.nstripes) {
         const int key0 = c * a.chunk;
         const int key1 = min(mb, key0 + a.chunk);
@@ -478,17 +540,7 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
             // the tile is given back after its last use: after every pass when the
             // chunk spans several sub-tiles (each pass reloads them), else after the last
             const bool release = nsub > 1 || hg + GP >= g;
-            // running max and sum of each head, kept (identically) by every thread
-            float m_run[GP], l_run[GP], alpha[GP];
-#pragma unroll
-            for (int gi = 0; gi < GP; ++gi) {
-                m_run[gi] = -INFINITY;
-                l_run[gi] = 0.f;
-            }
-            // two accumulators per head (even and odd keys): independent FMA chains
-            float4 acc[GP], acc2[GP];
-#pragma unroll
-            for (int gi = 0; gi < GP; ++gi) acc[gi] = acc2[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!run_stripe) reset();
 
             for (int st = 0; st < nsub; ++st) {
                 const int nk = min(C::TK, key1 - (key0 + st * C::TK));
@@ -685,43 +737,11 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
                 }
             }
             if (!ok) break;
-            // ---- combine the key groups and write the chunk partials (fp32, log2-domain lse)
-            float4* red4 = reinterpret_cast<float4*>(red);
-#pragma unroll
-            for (int gi = 0; gi < GP; ++gi) {
-                acc[gi].x += acc2[gi].x;
-                acc[gi].y += acc2[gi].y;
-                acc[gi].z += acc2[gi].z;
-                acc[gi].w += acc2[gi].w;
-            }
-            if (kq > 0) {
-#pragma unroll
-                for (int gi = 0; gi < GP; ++gi) red4[((kq - 1) * C::GMAX + gi) * C::NCG + cg] = acc[gi];
-            }
-            __syncthreads();
-            if (kq == 0) {
-#pragma unroll
-                for (int gi = 0; gi < GP; ++gi) {
-                    float4 t = acc[gi];
-#pragma unroll
-                    for (int u = 1; u < C::KQ; ++u) {
-                        const float4 o = red4[((u - 1) * C::GMAX + gi) * C::NCG + cg];
-                        t.x += o.x;
-                        t.y += o.y;
-                        t.z += o.z;
-                        t.w += o.w;
-                    }
-                    const int h = kvh * g + hg + gi;
-                    const size_t pr = (size_t(b) * a.Hq + h) * a.nc + c;
-                    const float inv = vscale / l_run[gi];
-                    reinterpret_cast<float4*>(a.o_part + pr * D)[cg] =
-                        make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
-                    if (cg == 0) a.lse_part[pr] = m_run[gi] + log2f(l_run[gi]);
-                }
-            }
-            __syncthreads();
+            // ---- the chunk partials of these heads (fp32, log2-domain lse)
+            if (!run_stripe) write_partial(hg, a.o_part, a.lse_part, a.nc, c);
         }
     }
+    if (run_stripe && ok) write_partial(0, a.g_o, a.g_lse, a.nstripes, stripe);
     // every issued copy must have landed before the CTA exits (only a wait that
     // gave up leaves any outstanding)
     if (tid == 0) {
@@ -730,7 +750,7 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
                             FA_SITE_DRAIN);
     }
     if constexpr (FUSED) {
-        fused_stripe_tail<D, T>(a, ok, b, kvh, stripe);
+        fused_stripe_tail<D, T>(a, ok, b, kvh, stripe, run_stripe);
     } else {
         // this CTA's partials are written: the merge grid may be scheduled
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
