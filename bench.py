@@ -478,7 +478,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=headline_ok,
                     help="the timed workload (the FP8 and paged decode workloads are timed "
                          "in the per-workload table)")
-    ap.add_argument("--profile", choices=["prefill", "backward", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "backward", "decode", "decode_single"],
+                    default=None,
                     help="run only --warmup + --steps calls of one operation on --workload "
                          "(or the long decode workload) and print nothing else: the "
                          "command the ncu summaries under profiles/ are taken with")
@@ -518,9 +519,9 @@ def main(argv=None):
         flush_read.max()
 
     if args.profile is not None:
-        wp = WORKLOADS[DECODE] if args.profile == "decode" and w.kind != "decode" else w
-        fn = {"prefill": bench_prefill, "backward": bench_backward,
-              "decode": bench_decode}[args.profile]
+        wp = WORKLOADS[DECODE] if args.profile.startswith("decode") and w.kind != "decode" else w
+        fn = {"prefill": bench_prefill, "backward": bench_backward, "decode": bench_decode,
+              "decode_single": bench_decode_single_launch}[args.profile]
         times = fn(torch, fa, wp, args.steps, args.warmup, flush, dist)
         if rank == 0:
             print(f"profile {args.profile} {wp.name}: {len(times)} timed calls, "

@@ -139,11 +139,14 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
  * errors as fa_decode; the chunk partials are merged by the chunk kernel
  * itself instead of a second kernel.  Each persistent CTA walks the chunks
  * s, s + S, s + 2S, ... of one (b, kv head) (S CTAs per (b, kv head), as many
- * as fit in one wave); once its chunks are done it merges their partials with
- * the LSE weights of "CUDA 实现 Flash Decoding" section 2.2 Step 2, and the last
- * of the S CTAs to finish merges the S results into o and lse (the merge is
- * associative, so the result is the same up to rounding order).  The page's
- * section 8 lists this single launch as its fourth lever.
+ * as fit in one wave) and merges its chunks with the LSE weights of "CUDA 实现
+ * Flash Decoding" section 2.2 Step 2.  When one pass over a K/V tile serves all
+ * query heads of the kv head (Hq/Hkv <= 4 for 16-bit inputs) it does so on the
+ * fly, carrying the running max, sum and accumulators from chunk to chunk; else
+ * it merges the chunk partials it wrote.  The last of the S CTAs to finish
+ * merges the S results into o and lse.  The merge is associative, so the result
+ * is the same up to rounding order.  The page's section 8 lists this single
+ * launch as its fourth lever.
  *
  * Workspace: the same per-(device, stream) buffer as fa_decode, plus room for
  * one merged result per CTA (at most B*Hq*nc*(d+1) fp32), plus B*Hkv int
