@@ -514,12 +514,14 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
         }
         __syncthreads();
     };
-    // Single launch with one pass over each tile (all g heads at once): the
-    // stripe's chunks are merged on the fly.  The running max, sum and
-    // accumulators carry on from one chunk to the next (Step 2's merge, done
-    // online), and only the stripe's own result is written.  Every stripe owns
-    // at least one chunk with keys (nstripes <= nc, contiguous K/V).
-    const bool run_stripe = FUSED && npass == 1;
+    // Single launch, or e4m3 K/V, with one pass over each tile (all g heads at
+    // once): the stripe's chunks are merged on the fly.  The running max, sum
+    // and accumulators carry on from one chunk to the next (Step 2's merge,
+    // done online), and only the stripe's own result is written: to the stripe
+    // partials of the single launch, or as partial `stripe` of nstripes for the
+    // merge kernel.  Every stripe owns at least one chunk with keys
+    // (nstripes <= nc, contiguous K/V).
+    const bool run_stripe = (FUSED || FP8) && npass == 1;
     if (run_stripe) reset();
 
     for (int c = stripe; c < a.nc && ok; c += a.nstripes) {
@@ -741,7 +743,8 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
             if (!run_stripe) write_partial(hg, a.o_part, a.lse_part, a.nc, c);
         }
     }
-    if (run_stripe && ok) write_partial(0, a.g_o, a.g_lse, a.nstripes, stripe);
+    if (run_stripe && ok)
+        write_partial(0, FUSED ? a.g_o : a.o_part, FUSED ? a.g_lse : a.lse_part, a.nstripes, stripe);
     // every issued copy must have landed before the CTA exits (only a wait that
     // gave up leaves any outstanding)
     if (tid == 0) {
@@ -790,7 +793,7 @@ bool encode_kv_maps(EncodeTiledFn enc, const void* k, const void* v, int Hkv, in
 
 template <int D, typename T, bool FP8, bool PAGED, int GP, bool FUSED>
 cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int* nstripes_out) {
     using C = DecodeCfg<D, T, FP8>;
     auto kern = chunk_kernel<D, T, FP8, PAGED, GP, FUSED>;
     const int g = a.Hq / a.Hkv;
@@ -827,21 +830,29 @@ cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     if (nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     DecodeArgs la = a;
     la.nstripes = int(nstripes);
+    *nstripes_out = la.nstripes;
     kern<<<dim3((unsigned)nblocks), dim3(C::THREADS), smem, stream>>>(tk, tv, la);
     return cudaGetLastError();
 }
 
 // The chunk kernel with GP dividing the GQA group, then (unless FUSED) the merge
 // kernel as a programmatic dependent, so that its launch overlaps the chunk
-// grid's tail; it waits for the data itself.
+// grid's tail; it waits for the data itself.  With e4m3 K/V and one pass per
+// tile (GP = g) the chunk kernel leaves one partial per stripe, so the merge
+// kernel combines nstripes partials per (b, h) instead of nc.
 template <int D, typename T, bool FP8, bool PAGED, bool FUSED>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                    cudaStream_t stream) {
     const int g = a.Hq / a.Hkv;
-    cudaError_t err = (g % 4 == 0)   ? launch_chunk<D, T, FP8, PAGED, 4, FUSED>(tk, tv, a, stream)
-                      : (g % 2 == 0) ? launch_chunk<D, T, FP8, PAGED, 2, FUSED>(tk, tv, a, stream)
-                                     : launch_chunk<D, T, FP8, PAGED, 1, FUSED>(tk, tv, a, stream);
+    const int gp = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
+    int nstripes = 0;
+    cudaError_t err =
+        gp == 4   ? launch_chunk<D, T, FP8, PAGED, 4, FUSED>(tk, tv, a, stream, &nstripes)
+        : gp == 2 ? launch_chunk<D, T, FP8, PAGED, 2, FUSED>(tk, tv, a, stream, &nstripes)
+                  : launch_chunk<D, T, FP8, PAGED, 1, FUSED>(tk, tv, a, stream, &nstripes);
     if (err != cudaSuccess || FUSED) return err;
+    DecodeArgs ma = a;
+    if (FP8 && gp == g) ma.nc = nstripes;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(a.B * a.Hq, D / 16);
     cfg.blockDim = dim3(128);
@@ -852,7 +863,7 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArg
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_kernel<D, T>, a);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<D, T>, ma);
 }
 
 }  // namespace dec

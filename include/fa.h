@@ -226,7 +226,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * exact attention over the dequantised cache
  *     K[b][j][h][:] = k_scale[h] * e4m3(k8[b][j][h][:]),
  *     V[b][j][h][:] = v_scale[h] * e4m3(v8[b][j][h][:]),
- * computed like fa_decode (same chunks, partials and merge).
+ * computed like fa_decode: the same chunks and the same LSE-weighted merge.
+ * When one pass over a K/V tile serves all query heads of a kv head
+ * (Hq/Hkv = 1, 2 or 4), each persistent chunk-kernel CTA merges its chunks on
+ * the fly (running max, sum and accumulators carried from chunk to chunk).  It
+ * leaves one partial per query head, and the merge kernel combines those few
+ * partials rather than one per chunk.  The merge is associative, so only the
+ * rounding order differs.
  *
  *   q, o, lse   as fa_decode; q and o are fp16 or bf16 (`dtype`).
  *   k8, v8      device, [B, M, Hkv, d] bytes, each an OCP e4m3 value (bias 7,
