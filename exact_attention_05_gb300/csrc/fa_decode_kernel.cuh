@@ -506,22 +506,23 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
                 }
                 const int h = kvh * g + hg + gi;
                 const size_t r = (size_t(b) * a.Hq + h) * per_head + idx;
-                const float inv = vscale / l_run[gi];
+                const bool empty = l_run[gi] == 0.f;  // no key reached this partial
+                const float inv = empty ? 0.f : vscale / l_run[gi];
                 reinterpret_cast<float4*>(o_dst + r * D)[cg] =
                     make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
-                if (cg == 0) lse_dst[r] = m_run[gi] + log2f(l_run[gi]);
+                if (cg == 0) lse_dst[r] = empty ? -INFINITY : m_run[gi] + log2f(l_run[gi]);
             }
         }
         __syncthreads();
     };
-    // Single launch, or e4m3 K/V, with one pass over each tile (all g heads at
-    // once): the stripe's chunks are merged on the fly.  The running max, sum
-    // and accumulators carry on from one chunk to the next (Step 2's merge,
-    // done online), and only the stripe's own result is written: to the stripe
-    // partials of the single launch, or as partial `stripe` of nstripes for the
-    // merge kernel.  Every stripe owns at least one chunk with keys
-    // (nstripes <= nc, contiguous K/V).
-    const bool run_stripe = (FUSED || FP8) && npass == 1;
+    // Single launch, e4m3 or paged K/V, with one pass over each tile (all g
+    // heads at once): the stripe's chunks are merged on the fly.  The running
+    // max, sum and accumulators carry on from one chunk to the next (Step 2's
+    // merge, done online), and only the stripe's own result is written: to the
+    // stripe partials of the single launch, or as partial `stripe` of nstripes
+    // for the merge kernel.  A paged stripe whose chunks all lie past its
+    // sequence's end leaves an empty partial (O = 0, lse = -inf).
+    const bool run_stripe = (FUSED || FP8 || PAGED) && npass == 1;
     if (run_stripe) reset();
 
     for (int c = stripe; c < a.nc && ok; c += a.nstripes) {
@@ -529,8 +530,9 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
         const int key1 = min(mb, key0 + a.chunk);
         if (key0 >= key1) {
             // a chunk past the end of a shorter (paged) sequence: an empty
-            // partial, which the merge weighs with 2^-inf = 0
-            for (int gi = 0; gi < g; ++gi) {
+            // partial, which the merge weighs with 2^-inf = 0 (nothing to add
+            // when the stripe merges on the fly)
+            for (int gi = 0; gi < g && !run_stripe; ++gi) {
                 const size_t pr = (size_t(b) * a.Hq + kvh * g + gi) * a.nc + c;
                 if (tid < NCP) reinterpret_cast<float2*>(a.o_part + pr * D)[tid] = make_float2(0.f, 0.f);
                 if (tid == 0) a.lse_part[pr] = -INFINITY;
@@ -837,9 +839,9 @@ cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
 
 // The chunk kernel with GP dividing the GQA group, then (unless FUSED) the merge
 // kernel as a programmatic dependent, so that its launch overlaps the chunk
-// grid's tail; it waits for the data itself.  With e4m3 K/V and one pass per
-// tile (GP = g) the chunk kernel leaves one partial per stripe, so the merge
-// kernel combines nstripes partials per (b, h) instead of nc.
+// grid's tail; it waits for the data itself.  With e4m3 or paged K/V and one
+// pass per tile (GP = g) the chunk kernel leaves one partial per stripe, so
+// the merge kernel combines nstripes partials per (b, h) instead of nc.
 template <int D, typename T, bool FP8, bool PAGED, bool FUSED>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                    cudaStream_t stream) {
@@ -852,7 +854,7 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArg
                   : launch_chunk<D, T, FP8, PAGED, 1, FUSED>(tk, tv, a, stream, &nstripes);
     if (err != cudaSuccess || FUSED) return err;
     DecodeArgs ma = a;
-    if (FP8 && gp == g) ma.nc = nstripes;
+    if ((FP8 || PAGED) && gp == g) ma.nc = nstripes;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(a.B * a.Hq, D / 16);
     cfg.blockDim = dim3(128);

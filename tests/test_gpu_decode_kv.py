@@ -140,7 +140,10 @@ def test_paged_decode_workload_full(oracle_mod):
 
 def test_paged_equals_contiguous_decode():
     """The same keys through a shuffled page pool and contiguously give the same
-    result up to the order of fp32 rounding inside a chunk (identical chunking)."""
+    result up to the order of fp32 rounding.  Both read the same rows into the
+    same tile positions; the paged path merges each stripe's chunks on the fly
+    and the contiguous two-kernel path merges per-chunk partials, which Step 2
+    of the flash-decoding page's section 2.2 makes the same sum in another order."""
     import exact_attention_05_gb300 as fa
     torch = torch_cuda()
     B, Hq, Hkv, M, d = 2, 8, 8, 4096, 128
@@ -151,9 +154,9 @@ def test_paged_equals_contiguous_decode():
                              d ** -0.5)
     o2, l2 = fa.decode(q.cuda(), k.cuda(), v.cuda(), 128, d ** -0.5)
     torch.cuda.synchronize()
-    # both read the same rows into the same tile positions: bitwise equal
-    assert torch.equal(o1, o2)
-    assert torch.equal(l1, l2)
+    # a few fp32 roundings of the merge apart: far below the parity tolerances
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-4
+    assert (l1 - l2).abs().max().item() <= 2e-5
 
 
 def test_paged_decode_rejects_bad_geometry():
