@@ -253,7 +253,10 @@ fa_status fa_decode_fp8(const void* q, const void* k8, const void* v8, const flo
  * "TODO" section of "[CUDA 优化实战] fmha sm120 : 超越
  * torch.sdpa(flash-attention-2)", "attention with kv cache block").  Key j of
  * sequence b is row j % page_size of page block_table[b][j / page_size]; the
- * result is fa_decode's on the gathered K/V of the first seq_lens[b] keys.
+ * result is fa_decode's on the gathered K/V of the first seq_lens[b] keys, up
+ * to rounding order.  As in fa_decode_fp8, when Hq/Hkv is 1, 2 or 4 each
+ * persistent chunk-kernel CTA merges its chunks on the fly, and the merge
+ * kernel combines one partial per CTA.
  *
  *   q, o, lse          as fa_decode (one query row per (b, h)).
  *   k_cache, v_cache   device, [num_pages, page_size, Hkv, d] of `dtype`,
