@@ -312,7 +312,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
 // TMA copies of the K and V sub-tiles, in the order the chunks consume them,
 // into a ring of tile slots, and refills a slot as soon as the last pass over
 // it is done, so the next tiles stream in while the current one is computed.
-// Each chunk still yields its own partial (O_c, lse_c), as in Step 1.
+// On the 16-bit two-kernel path (and whenever a tile takes several passes)
+// each chunk yields its own partial (O_c, lse_c), as in Step 1; otherwise a
+// stripe's chunks are merged on the fly into one partial per stripe.
 template <int D, typename T, bool FP8, bool PAGED, int GP, bool FUSED>
 __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
