@@ -12,8 +12,11 @@
 // discussion, so that most tiles touch O not at all.
 //
 // How it runs on GB300 (not the page's design, which used ldmatrix + mma.sync):
-//   * one CTA per pair of 128-row Q tiles of one (b, h) -- 256 query rows --
-//     sharing every K/V tile; 10 warps with fixed roles:
+//   * one CTA per pair of 128-row Q tiles sharing every K/V tile: rows r and
+//     r + 128 of one (b, h), or -- causal with an even GQA group -- the same
+//     128 rows of query heads h and h + 1, which read the same kv head and
+//     so walk the same causal key range (no lone last KV tile for tile 1);
+//     10 warps with fixed roles:
 //       warps 0-3  softmax of Q tile 0, warps 4-7 softmax of Q tile 1: thread
 //                  t of a warpgroup owns query row t of its tile (TMEM lane
 //                  t); it reads its S row from TMEM, masks, updates m/l,
@@ -95,7 +98,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const PrefillArgs a) {
+                   const PrefillArgs a, const int pair_heads) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -109,19 +112,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Which pair of Q tiles: the latest (most expensive, when causal) pairs go first.
-    const int npairs = (a.n_qtiles + 1) / 2;
-    const int nbh = a.B * a.Hq;
+    // Which pair of Q tiles: the latest (most expensive, when causal) pairs go
+    // first.  Tile i covers query head h + i*dh, rows q0 + i*dr: consecutive
+    // rows of one head, or (pair_heads) the same rows of two heads.
+    const int dh = pair_heads ? 1 : 0;
+    const int dr = pair_heads ? 0 : C::BM;
+    const int nrow = pair_heads ? a.n_qtiles : (a.n_qtiles + 1) / 2;  // row positions
+    const int nhu = pair_heads ? a.Hq / 2 : a.Hq;                      // head units
+    const int nbh = a.B * nhu;
     const int lin = blockIdx.x;
-    const int pt = npairs - 1 - lin / nbh;
+    const int pt = nrow - 1 - lin / nbh;
     const int bh = lin % nbh;
-    const int h = bh % a.Hq;
-    const int b = bh / a.Hq;
+    const int h = (bh % nhu) * (1 + dh);  // query head of tile 0
+    const int b = bh / nhu;
     const int kvh = h / (a.Hq / a.Hkv);
-    const int q0 = pt * (C::NQ * C::BM);
-    const bool t1 = q0 + C::BM < a.N;  // is Q tile 1 inside the sequence?
+    const int q0 = pt * (C::BM + dr);
+    const bool t1 = pair_heads || q0 + C::BM < a.N;  // does Q tile 1 exist?
     auto ntiles = [&](int i) -> int {
-        const int kv_end = a.causal ? min(a.M, q0 + (i + 1) * C::BM) : a.M;
+        const int kv_end = a.causal ? min(a.M, q0 + i * dr + C::BM) : a.M;
         return (kv_end + C::BN - 1) / C::BN;
     };
     const int nt0 = ntiles(0);
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int s = 0; s < C::NSUB; ++s)
                     tma_load_4d(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64,
-                                h, q0 + i * C::BM, b, full);
+                                h + i * dh, q0 + i * dr, b, full);
             };
             load_q(0, bar(C::B_QFULL));
             bool q1_issued = false;
@@ -328,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------- softmax
         const int tile = warp >> 2;  // 0 or 1
         const int r = threadIdx.x & 127;  // row in tile == TMEM lane
-        const int row0 = q0 + tile * C::BM;
+        const int row0 = q0 + tile * dr;
+        const int ht = h + tile * dh;  // this tile's query head
         const int row = row0 + r;
         const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
         const int nti = tile == 0 ? nt0 : nt;
@@ -466,13 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (a.lse != nullptr && row < a.N)
-                a.lse[(size_t(b) * a.Hq + h) * a.N + row] = (m_ref + log2f(l)) * kLn2;
+                a.lse[(size_t(b) * a.Hq + ht) * a.N + row] = (m_ref + log2f(l)) * kLn2;
         }
         fence_async_shared();
         named_barrier_sync(1 + tile, 128);
         if (r == 0 && ok && *abort_flag == 0) {
             for (int s = 0; s < C::NSUB; ++s)
-                tma_store_4d(&tm_o, smem_addr(stage) + s * C::SUB_BYTES, s * 64, h, row0, b);
+                tma_store_4d(&tm_o, smem_addr(stage) + s * C::SUB_BYTES, s * 64, ht, row0, b);
             tma_store_commit();
             tma_store_wait_all();
         }
@@ -495,9 +504,13 @@ cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    const long long nblocks = (long long)((a.n_qtiles + 1) / 2) * a.B * a.Hq;
+    // causal with an even GQA group: pair the same rows of two query heads
+    const int pair_heads = (a.causal && (a.Hq / a.Hkv) % 2 == 0) ? 1 : 0;
+    const long long nblocks = pair_heads ? (long long)a.n_qtiles * a.B * (a.Hq / 2)
+                                         : (long long)((a.n_qtiles + 1) / 2) * a.B * a.Hq;
     if (nblocks <= 0 || nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<dim3((unsigned)nblocks), dim3(kThreads), C::SMEM_BYTES, stream>>>(tq, tk, tv, to, a);
+    kern<<<dim3((unsigned)nblocks), dim3(kThreads), C::SMEM_BYTES, stream>>>(tq, tk, tv, to, a,
+                                                                           pair_heads);
     return cudaGetLastError();
 }
 
