@@ -64,3 +64,30 @@ def test_single_process_helpers():
     assert bench.init_dist(1, "gloo") is None
     assert bench.max_over_ranks(3.5, None) == 3.5
     assert bench.aggregate_throughput(8.0, 1, 2.0) == 4.0
+
+
+def test_source_digest_ignores_comments_only():
+    """A recorded ncu traffic figure stays valid across comment edits and is
+    dropped (null) once the code of the kernel's sources changes."""
+    import bench
+    code = "int f(int x) {\n    return x + 1;  // add one\n}\n/* block\n   comment */\n"
+    assert bench._code_only(code) == bench._code_only(code.replace("add one", "increment"))
+    assert bench._code_only(code) == bench._code_only("// header\n" + code + "\n\n")
+    assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))
+    assert "//" not in bench._code_only(code) and "/*" not in bench._code_only(code)
+
+
+def test_recorded_traffic_lines_parse():
+    """Every line of the committed traffic record names a known kernel and a
+    positive byte count; a line whose digest no longer matches reads as None."""
+    import os
+    import bench
+    path = os.path.join(bench.ROOT, "profiles", "ncu_traffic.txt")
+    lines = [l.split() for l in open(path).read().splitlines() if l.strip() and not l.startswith("#")]
+    assert lines
+    for workload, kernel, digest, nbytes in lines:
+        assert kernel in bench.KERNEL_SOURCES
+        assert len(digest) == 16 and float(nbytes) > 0
+        got = bench.recorded_traffic(workload, kernel)
+        assert got is None or got == float(nbytes)
+    assert bench.recorded_traffic("no_such_workload", "prefill_kernel") is None
