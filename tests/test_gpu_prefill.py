@@ -33,6 +33,9 @@ CASES = [
     (1, 3, 3, 384, 384, 128, FP16, False),
     (2, 4, 2, 384, 384, 128, BF16, True),
     (1, 2, 2, 127, 129, 64, FP16, True),
+    # causal with an even GQA group (two query heads per CTA) and N != M
+    (1, 4, 2, 130, 400, 128, FP16, True),
+    (2, 8, 2, 400, 131, 64, BF16, True),
 ]
 
 
