@@ -7,7 +7,8 @@ decode as fa_decode but keeps the chunk partials in a fixed array of static
 device memory instead of an allocated workspace.  Here it is called through the
 C ABI and compared with fa_decode on two calls in a row (different shapes, so a
 stale partial left in the shared array by the first call would show up in the
-second), within the tolerances the other parity tests use.
+second), within the tolerances the other parity tests use, and once captured
+inside a CUDA graph and replayed.
 
 The file name makes pytest collect it last.
 """
@@ -56,3 +57,36 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     st = fa.fa_decode_noalloc(q, k, k, q, None, 4, 32, 32, 8192, 128, 16, 0.1, FP16, check=False)
     assert st == fa.FA_ERR_SCRATCH_LIMIT
     assert "scratch" in fa.fa_status_string(st)
+
+
+def test_noalloc_decode_inside_a_captured_cuda_graph(lib):
+    """Captured once into a CUDA graph (capture fails on any allocation), then
+    replayed with new query values written into the same buffer: every replay
+    must equal an eager fa_decode on those values."""
+    torch = torch_cuda()
+    B, Hq, Hkv, M, d, chunk = 2, 8, 2, 3000, 128, 128
+    scale = 1.0 / d ** 0.5
+    q0, k, v = (t.cuda() for t in make_inputs(B, Hq, Hkv, 1, M, d, FP16, seed=71))
+    q = q0.clone()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first call (looks up the array) before any capture
+        fa.fa_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, FP16, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fa.fa_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, M, d, chunk, scale, FP16)
+    for seed in (72, 73):
+        qn, _, _ = make_inputs(B, Hq, Hkv, 1, M, d, FP16, seed=seed)
+        q.copy_(qn.cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        o_ref, lse_ref = fa.decode(q, k, v, chunk, scale)
+        torch.cuda.synchronize()
+        eo = (o.double() - o_ref.double()).abs().max().item()
+        el = (lse.double() - lse_ref.double()).abs().max().item()
+        assert eo <= O_TOL[FP16] and el <= LSE_TOL, (seed, eo, el)
+    assert fa.fa_get_last_device_status() == fa.FA_OK
