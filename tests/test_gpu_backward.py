@@ -93,12 +93,31 @@ def test_backward_deterministic_dk_dv():
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
-@pytest.mark.parametrize("name", ["prefill_causal_gqa32x8_n8192_f16_peaky",
-                                  "prefill_causal_h16_n32768_bf16"])
+def test_backward_gqa_workload_full(oracle_mod):
+    """The causal GQA workload (Hq=32, Hkv=8, N=M=8192, fp16, 1% of K rows x8) as the
+    bench runs its backward, every element of dQ, dK and dV against the oracle."""
+    from exact_attention_05_gb300.workloads import WORKLOADS, workload_inputs
+    w = WORKLOADS["prefill_causal_gqa32x8_n8192_f16_peaky"]
+    q, k, v = workload_inputs(w)
+    dout = make_dout(w.B, w.N, w.Hq, w.d, w.dtype, w.seed + 7)
+    got = run_backward(q, k, v, dout, w.causal, w.scale)
+    ref = oracle_mod.attention_backward(bits(q), bits(k), bits(v), bits(dout), w.dtype, w.causal,
+                                        w.scale)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert np.isfinite(g).all(), f"{name}: non-finite"
+        e = float(np.abs(g - r).max())
+        scl = max(float(np.abs(r).max()), 1.0)
+        print(f"PARITY backward {w.name} {name}: max|err| = {e:.3e}, scale {scl:.3e}")
+        assert e <= TOL[w.dtype] * scl, f"{name}: max|err| {e:.3e} > {TOL[w.dtype]:.1e} * {scl:.3e}"
+
+
+@pytest.mark.parametrize("name", ["prefill_causal_h16_n32768_bf16"])
 def test_backward_workload_full_sampled(oracle_mod, name):
-    """The two large prefill workloads at full size, as the bench runs their backward:
-    dQ on sampled rows against the oracle (dQ_i depends on row i alone), and dK, dV
-    through properties that hold at any size: sum_j dK_j = 0 for every (b, kv head)
+    """The long causal workload at full size, as the bench runs its backward (its
+    full fp64 backward would take the oracle several minutes on 16 cores, as it is
+    parallel over (b, kv head) only): dQ on sampled rows against the oracle (dQ_i
+    depends on row i alone), and dK, dV through properties that hold at any size:
+    sum_j dK_j = 0 for every (b, kv head)
     (the softmax ignores a common shift of the keys), and sum_j dV_j equals the sum of
     dO over the rows of the query heads that read the kv head (every P row sums to 1).
     The sums are checked within 8 ulp of the type times sum_j |dK_j| (resp. |dV_j|),
