@@ -93,12 +93,15 @@ struct PrefillCfg {
 constexpr int kThreads = 320;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+// K/V bytes of the heads whose CTAs are dispatched together: half the 129 MB L2,
+// leaving room for the Q and O tiles streaming through it.
+constexpr double kL2GroupBytes = 64.0 * 1024 * 1024;
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const PrefillArgs a, const int pair_heads) {
+                   const PrefillArgs a, const int pair_heads, const int ngroups) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -112,17 +115,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Which pair of Q tiles: the latest (most expensive, when causal) pairs go
-    // first.  Tile i covers query head h + i*dh, rows q0 + i*dr: consecutive
-    // rows of one head, or (pair_heads) the same rows of two heads.
+    // Which pair of Q tiles.  Tile i covers query head h + i*dh, rows q0 + i*dr:
+    // consecutive rows of one head, or (pair_heads) the same rows of two heads.
+    // The head units (b, query head or head pair) are cut into `ngroups`
+    // consecutive groups of balanced size whose K/V fit in L2 together.  The
+    // groups are dispatched one after the other; inside a group the latest
+    // (most expensive, when causal) row positions go first, head units
+    // fastest, so the CTAs resident at one time read the K/V of few heads.
     const int dh = pair_heads ? 1 : 0;
     const int dr = pair_heads ? 0 : C::BM;
     const int nrow = pair_heads ? a.n_qtiles : (a.n_qtiles + 1) / 2;  // row positions
     const int nhu = pair_heads ? a.Hq / 2 : a.Hq;                      // head units
     const int nbh = a.B * nhu;
     const int lin = blockIdx.x;
-    const int pt = nrow - 1 - lin / nbh;
-    const int bh = lin % nbh;
+    const int gbase = nbh / ngroups, grem = nbh % ngroups;  // groups 0..grem-1 hold gbase + 1
+    const int u = lin / nrow;
+    const int grp = u < (gbase + 1) * grem ? u / (gbase + 1) : grem + (u - (gbase + 1) * grem) / gbase;
+    const int gstart = grp * gbase + min(grp, grem);
+    const int gsize = gbase + (grp < grem ? 1 : 0);
+    const int gr = lin - gstart * nrow;
+    const int pt = nrow - 1 - gr / gsize;
+    const int bh = gstart + gr % gsize;
     const int h = (bh % nhu) * (1 + dh);  // query head of tile 0
     const int b = bh / nhu;
     const int kvh = h / (a.Hq / a.Hkv);
@@ -169,11 +182,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // Q0 and K0 first: the first QK needs nothing else; Q1 follows on its own
             // barrier (the first wave's loads all go out at once, so order matters)
+            // Q is read once: it leaves L2 before the K/V tiles other CTAs reuse
+            const uint64_t once = l2_policy_evict_first();
             auto load_q = [&](int i, uint32_t full) {
                 mbar_arrive_expect_tx(full, C::TILE_BYTES);
                 for (int s = 0; s < C::NSUB; ++s)
-                    tma_load_4d(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64,
-                                h + i * dh, q0 + i * dr, b, full);
+                    tma_load_4d_hint(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q,
+                                     s * 64, h + i * dh, q0 + i * dr, b, full, once);
             };
             load_q(0, bar(C::B_QFULL));
             bool q1_issued = false;
@@ -480,8 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_shared();
         named_barrier_sync(1 + tile, 128);
         if (r == 0 && ok && *abort_flag == 0) {
+            const uint64_t once = l2_policy_evict_first();  // O is not read again here
             for (int s = 0; s < C::NSUB; ++s)
-                tma_store_4d(&tm_o, smem_addr(stage) + s * C::SUB_BYTES, s * 64, ht, row0, b);
+                tma_store_4d_hint(&tm_o, smem_addr(stage) + s * C::SUB_BYTES, s * 64, ht, row0, b,
+                                  once);
             tma_store_commit();
             tma_store_wait_all();
         }
@@ -501,16 +518,21 @@ cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const
                              const CUtensorMap& to, const PrefillArgs& a, cudaStream_t stream) {
     using C = PrefillCfg<D>;
     auto kern = prefill_kernel<D, T>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::SMEM_BYTES);
+    static std::atomic<unsigned> configured{0};
+    cudaError_t err = configure_kernel_once(kern, configured);
     if (err != cudaSuccess) return err;
     // causal with an even GQA group: pair the same rows of two query heads
     const int pair_heads = (a.causal && (a.Hq / a.Hkv) % 2 == 0) ? 1 : 0;
-    const long long nblocks = pair_heads ? (long long)a.n_qtiles * a.B * (a.Hq / 2)
-                                         : (long long)((a.n_qtiles + 1) / 2) * a.B * a.Hq;
+    const long long nbh = (long long)a.B * (pair_heads ? a.Hq / 2 : a.Hq);
+    const long long nblocks = pair_heads ? (long long)a.n_qtiles * nbh
+                                         : (long long)((a.n_qtiles + 1) / 2) * nbh;
     if (nblocks <= 0 || nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // L2 groups: as many as it takes for each group's K/V to fit in kL2GroupBytes
+    const double kv_bytes = 2.0 * a.M * D * sizeof(T) * (double)a.B * a.Hkv;
+    long long ngroups = (long long)std::ceil(kv_bytes / kL2GroupBytes);
+    ngroups = ngroups < 1 ? 1 : (ngroups > nbh ? nbh : ngroups);
     kern<<<dim3((unsigned)nblocks), dim3(kThreads), C::SMEM_BYTES, stream>>>(tq, tk, tv, to, a,
-                                                                           pair_heads);
+                                                                           pair_heads, (int)ngroups);
     return cudaGetLastError();
 }
 
