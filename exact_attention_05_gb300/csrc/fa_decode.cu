@@ -77,6 +77,26 @@ cudaError_t launch_decode_fused(const CUtensorMap& tk, const CUtensorMap& tv, co
     return cudaErrorInvalidValue;
 }
 
+cudaError_t prepare_decode_kernels() {
+    cudaError_t err = cudaSuccess;
+    auto one = [&](cudaError_t e) {
+        if (err == cudaSuccess) err = e;
+    };
+    one(dec::configure_chunk<128, __half, false, false, 1, false>());
+    one(dec::configure_chunk<128, __half, false, false, 2, false>());
+    one(dec::configure_chunk<128, __half, false, false, 4, false>());
+    one(dec::configure_chunk<128, __nv_bfloat16, false, false, 1, false>());
+    one(dec::configure_chunk<128, __nv_bfloat16, false, false, 2, false>());
+    one(dec::configure_chunk<128, __nv_bfloat16, false, false, 4, false>());
+    one(dec::configure_chunk<64, __half, false, false, 1, false>());
+    one(dec::configure_chunk<64, __half, false, false, 2, false>());
+    one(dec::configure_chunk<64, __half, false, false, 4, false>());
+    one(dec::configure_chunk<64, __nv_bfloat16, false, false, 1, false>());
+    one(dec::configure_chunk<64, __nv_bfloat16, false, false, 2, false>());
+    one(dec::configure_chunk<64, __nv_bfloat16, false, false, 4, false>());
+    return err;
+}
+
 cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cudaStream_t stream) {
     wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
     return cudaGetLastError();

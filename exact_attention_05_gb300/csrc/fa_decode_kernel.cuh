@@ -23,10 +23,11 @@
 //   * scores: thread <-> key, the full dot product read from a swizzled K
 //     tile (one 16-byte chunk per step, conflict-free); softmax in registers
 //     with warp-shuffle reductions; P.V: thread <-> (4 columns, key group).
-//   * the merge: a second kernel (one CTA per (b, h) and 16 columns), or, in
-//     the single launch, each stripe CTA merges its own chunks (on the fly,
-//     when one pass over a tile serves all its query heads) and the last
-//     stripe of a (b, kv head) merges the stripes.
+//   * the merge: each stripe CTA merges its own chunks on the fly when one
+//     pass over a tile serves all its query heads (else it writes one partial
+//     per chunk); then a second kernel (one CTA per (b, h) and 16 columns)
+//     merges the stripes' partials, or, in the single launch, the last stripe
+//     of a (b, kv head) does.
 //   * e4m3 K/V: the same tiles at one byte per element; the per-kv-head scales
 //     are applied once per score (s = k_scale * q.k8) and once per output
 //     (o = v_scale * sum_j p_j v8_j), which is exact algebra.
@@ -312,9 +313,10 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
 // TMA copies of the K and V sub-tiles, in the order the chunks consume them,
 // into a ring of tile slots, and refills a slot as soon as the last pass over
 // it is done, so the next tiles stream in while the current one is computed.
-// On the 16-bit two-kernel path (and whenever a tile takes several passes)
-// each chunk yields its own partial (O_c, lse_c), as in Step 1; otherwise a
-// stripe's chunks are merged on the fly into one partial per stripe.
+// When one pass over a tile serves every query head of the group (g <= 4),
+// a stripe's chunks are merged on the fly into one partial per stripe;
+// otherwise (several passes per tile) each chunk yields its own partial
+// (O_c, lse_c), as in Step 1.
 template <int D, typename T, bool FP8, bool PAGED, int GP, bool FUSED>
 __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -517,14 +519,14 @@ __global__ void __launch_bounds__(128, (FP8 && GP == 1) ? 5 : 3)
         }
         __syncthreads();
     };
-    // Single launch, e4m3 or paged K/V, with one pass over each tile (all g
-    // heads at once): the stripe's chunks are merged on the fly.  The running
-    // max, sum and accumulators carry on from one chunk to the next (Step 2's
-    // merge, done online), and only the stripe's own result is written: to the
-    // stripe partials of the single launch, or as partial `stripe` of nstripes
-    // for the merge kernel.  A paged stripe whose chunks all lie past its
-    // sequence's end leaves an empty partial (O = 0, lse = -inf).
-    const bool run_stripe = (FUSED || FP8 || PAGED) && npass == 1;
+    // With one pass over each tile (all g heads at once) the stripe's chunks
+    // are merged on the fly.  The running max, sum and accumulators carry on
+    // from one chunk to the next (Step 2's merge, done online), and only the
+    // stripe's own result is written: to the stripe partials of the single
+    // launch, or as partial `stripe` of nstripes for the merge kernel.  A
+    // paged stripe whose chunks all lie past its sequence's end leaves an
+    // empty partial (O = 0, lse = -inf).
+    const bool run_stripe = npass == 1;
     if (run_stripe) reset();
 
     for (int c = stripe; c < a.nc && ok; c += a.nstripes) {
@@ -795,6 +797,18 @@ bool encode_kv_maps(EncodeTiledFn enc, const void* k, const void* v, int Hkv, in
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Dynamic shared memory a chunk kernel may need (227 KB, less its static
+// shared memory, is what the device allows; a launch beyond it is refused).
+constexpr size_t kMaxChunkSmem = size_t(227) * 1024;
+
+// Launch attributes of one chunk-kernel variant, set once per device, so that
+// a launch of any GQA group size needs no further set-up.
+template <int D, typename T, bool FP8, bool PAGED, int GP, bool FUSED>
+cudaError_t configure_chunk() {
+    static std::atomic<unsigned> configured{0};
+    return configure_kernel_once(chunk_kernel<D, T, FP8, PAGED, GP, FUSED>, configured);
+}
+
 template <int D, typename T, bool FP8, bool PAGED, int GP, bool FUSED>
 cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                          cudaStream_t stream, int* nstripes_out) {
@@ -802,12 +816,8 @@ cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     auto kern = chunk_kernel<D, T, FP8, PAGED, GP, FUSED>;
     const int g = a.Hq / a.Hkv;
     const size_t smem = C::smem_bytes(g);
-    if (smem > size_t(227) * 1024) return cudaErrorInvalidConfiguration;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(smem));
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               int(cudaSharedmemCarveoutMaxShared));
+    if (smem > kMaxChunkSmem) return cudaErrorInvalidConfiguration;
+    cudaError_t err = configure_chunk<D, T, FP8, PAGED, GP, FUSED>();
     if (err != cudaSuccess) return err;
     // resident CTAs per SM for this shared-memory size (cached: it depends on g only)
     static std::atomic<long long> cached{-1};
@@ -841,9 +851,9 @@ cudaError_t launch_chunk(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
 
 // The chunk kernel with GP dividing the GQA group, then (unless FUSED) the merge
 // kernel as a programmatic dependent, so that its launch overlaps the chunk
-// grid's tail; it waits for the data itself.  With e4m3 or paged K/V and one
-// pass per tile (GP = g) the chunk kernel leaves one partial per stripe, so
-// the merge kernel combines nstripes partials per (b, h) instead of nc.
+// grid's tail; it waits for the data itself.  With one pass per tile (GP = g)
+// the chunk kernel leaves one partial per stripe, so the merge kernel
+// combines nstripes partials per (b, h) instead of nc.
 template <int D, typename T, bool FP8, bool PAGED, bool FUSED>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                    cudaStream_t stream) {
@@ -856,7 +866,7 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArg
                   : launch_chunk<D, T, FP8, PAGED, 1, FUSED>(tk, tv, a, stream, &nstripes);
     if (err != cudaSuccess || FUSED) return err;
     DecodeArgs ma = a;
-    if ((FP8 || PAGED) && gp == g) ma.nc = nstripes;
+    if (gp == g) ma.nc = nstripes;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(a.B * a.Hq, D / 16);
     cfg.blockDim = dim3(128);
