@@ -2,6 +2,11 @@
 // checks (all of them before any CUDA call), per-device state (architecture
 // check, device status word, decode workspaces), TMA tensor-map encoding and
 // the kernel launches.
+//
+// The status word that every kernel's bounded waits report to is static
+// device memory (g_status_word below): each device that loads the module
+// holds its own, zero at load, and finding its address allocates nothing, so
+// the allocation-free decode shares it with every other entry point.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -22,6 +27,10 @@ namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+
+// One status word per device: the low byte FA_DEV_TIMEOUT (or FA_DEV_LAYOUT),
+// the next byte the wait site; zero when nothing went wrong.
+static __device__ int g_status_word;
 
 struct Workspace {
     void* ptr = nullptr;
@@ -77,7 +86,7 @@ fa_status check_args(const void* q, const void* k, const void* v, const void* o,
     return FA_OK;
 }
 
-// Current device's state; checks the architecture once and creates the status word.
+// Current device's state; checks the architecture and looks up the status word once.
 fa_status device_state(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -90,10 +99,12 @@ fa_status device_state(DeviceState** out) {
             return FA_ERR_CUDA;
         st.supported = (major == 10 && minor == 3);
         if (st.supported) {
-            if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return FA_ERR_NO_MEMORY;
-            if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess ||
-                cudaDeviceSynchronize() != cudaSuccess)
+            // the host-side name of the word is not its device address: look the
+            // address up on this device (with it current)
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || p == nullptr)
                 return FA_ERR_CUDA;
+            st.status = static_cast<int*>(p);
         }
         st.checked = true;
     }
@@ -210,6 +221,17 @@ fa_status decode_setup(DeviceState* st, cudaStream_t stream, const void* q, void
 }
 
 }  // namespace
+
+namespace fa {
+
+int* status_word_current_device() {
+    DeviceState* st = nullptr;
+    return device_state(&st) == FA_OK ? st->status : nullptr;
+}
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+
+}  // namespace fa
 
 FA_EXPORT fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                            int Hq, int Hkv, int N, int M, int d, int causal, float scale,

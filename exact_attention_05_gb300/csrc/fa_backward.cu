@@ -612,7 +612,8 @@ cudaError_t launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     auto kern = backward_kernel<D, T>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    static std::atomic<unsigned> configured{0};
+    err = configure_kernel_once(kern, configured);
     if (err != cudaSuccess) return err;
     const long long nblocks = (long long)a.n_ktiles * a.B * a.Hkv;
     if (nblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

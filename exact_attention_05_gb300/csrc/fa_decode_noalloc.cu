@@ -13,16 +13,20 @@
 //
 // Rules of use:
 //   * the first call on a device resolves the array's device address with
-//     cudaGetSymbolAddress (once per device, with that device current); make
-//     that first call before any stream capture begins;
+//     cudaGetSymbolAddress (once per device, with that device current), looks
+//     up the library's status word the same way and applies the launch
+//     attributes of every decode kernel variant; make that first call before
+//     any stream capture begins;
 //   * problems that need more than FA_DECODE_NOALLOC_SCRATCH_BYTES of
 //     partials are rejected with FA_ERR_SCRATCH_LIMIT before any launch;
 //   * every call shares the one array and it keeps the previous call's
 //     contents; the chunk kernel writes every partial before the merge reads
 //     it, so nothing has to be cleared -- but calls that overlap on the GPU
 //     (different streams, no ordering between them) race on the array;
-//   * bounded-wait timeouts of these launches are recorded in a status word
-//     of this file, not in the one fa_get_last_device_status() reads.
+//   * the kernels' bounded waits take the limit fa_set_wait_timeout_ns() set
+//     (read at each call) and report an expiry in the library's status word,
+//     the one fa_get_last_device_status() reads and clears; that word is
+//     static device memory too.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -40,7 +44,6 @@ namespace {
 constexpr size_t kScratchFloats = FA_DECODE_NOALLOC_SCRATCH_BYTES / sizeof(float);
 
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
-static __device__ int g_noalloc_status;
 
 using fa::EncodeTiledFn;
 
@@ -56,13 +59,13 @@ DeviceSetup g_setup[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 std::mutex g_mu;
 
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr uint64_t kMaxElements = 1ull << 39;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // One-time set-up of the current device: architecture check, the device
-// addresses of the static array and status word, the tensor-map encoder.
+// addresses of the static array and of the status word, the tensor-map
+// encoder, the decode kernels' launch attributes.
 fa_status setup_current_device(DeviceSetup** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -78,13 +81,13 @@ fa_status setup_current_device(DeviceSetup** out) {
             s.result = FA_ERR_UNSUPPORTED;
         } else {
             void* p = nullptr;
-            void* st = nullptr;
+            int* st = fa::status_word_current_device();
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr ||
-                cudaGetSymbolAddress(&st, g_noalloc_status) != cudaSuccess || st == nullptr) {
+                st == nullptr || fa::prepare_decode_kernels() != cudaSuccess) {
                 s.result = FA_ERR_CUDA;
             } else {
                 s.scratch = static_cast<float*>(p);
-                s.status = static_cast<int*>(st);
+                s.status = st;
                 s.result = FA_OK;
             }
         }
@@ -147,7 +150,7 @@ FA_EXPORT fa_status fa_decode_noalloc(const void* q, const void* k, const void* 
     a.nc = (int)nc;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.status = s->status;
-    a.timeout_ns = kTimeoutNs;
+    a.timeout_ns = fa::wait_timeout_ns();
     return fa::launch_decode(tk, tv, a, d, (int)dtype, (cudaStream_t)stream) == cudaSuccess
                ? FA_OK
                : FA_ERR_CUDA;

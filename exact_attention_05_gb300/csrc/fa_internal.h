@@ -3,6 +3,7 @@
 // the public ABI; include/fa.h is.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -126,6 +127,49 @@ cudaError_t launch_decode_fused(const CUtensorMap& tk, const CUtensorMap& tv, co
                                 int d, int dtype, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cudaStream_t stream);
+
+// The library's status word on the current device: static device memory
+// (every device that loads the module holds one, zero at load), so looking
+// it up allocates nothing.  Resolved once per device with cudaGetSymbolAddress.
+// Returns nullptr if the lookup failed.
+int* status_word_current_device();
+
+// The current limit of every device-side wait (fa_set_wait_timeout_ns).
+unsigned long long wait_timeout_ns();
+
+// Sets a kernel's launch attributes once per device: the largest dynamic
+// shared memory the device allows next to the kernel's static shared memory
+// (so that a launch of any size up to that needs no further set-up), and the
+// largest shared-memory carveout.  `configured` is the caller's per-kernel
+// record of the devices done (bit i = device i; devices from 32 on are
+// configured on every call).
+template <typename Kernel>
+cudaError_t configure_kernel_once(Kernel kern, std::atomic<unsigned>& configured) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const unsigned bit = dev < 32 ? (1u << dev) : 0u;
+    if (bit != 0u && (configured.load(std::memory_order_acquire) & bit) != 0u) return cudaSuccess;
+    cudaFuncAttributes fattr{};
+    int optin = 0;
+    if ((err = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+        cudaSuccess)
+        return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               optin - int(fattr.sharedSizeBytes));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               int(cudaSharedmemCarveoutMaxShared));
+    if (err != cudaSuccess) return err;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
+
+// Applies the launch attributes of every two-kernel 16-bit decode variant on
+// the current device (all head dims, types and heads-per-pass), so that
+// later calls configure nothing.
+cudaError_t prepare_decode_kernels();
 
 // Geometry the host needs to build tensor maps.
 constexpr int kPrefillTile = 128;   // query rows per tile and keys per KV tile

@@ -174,14 +174,17 @@ fa_status fa_decode_fused(const void* q, const void* k, const void* v, void* o, 
  * d=128 needs 4.2 MB).  The call makes no cudaMalloc, cudaFree or other
  * allocating call.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, once per device, with that device current): make
- * that first call before any stream capture starts.  All calls share the one
- * array and it keeps the previous call's contents; nothing in it needs to
- * start at zero, but calls that overlap on the GPU (e.g. on two streams with
- * no ordering between them) race on it and give undefined results.  Device
- * wait timeouts of these launches are recorded in a status word of their
- * own, not the one fa_get_last_device_status() reads.
+ * The first call on a device looks up the array's device address and that
+ * of the library's status word (cudaGetSymbolAddress, once per device, with
+ * that device current) and applies the launch attributes of every decode
+ * kernel variant (each head dim, type and GQA group): make that first call
+ * before any stream capture starts.  All calls share the one array and it
+ * keeps the previous call's contents; nothing in it needs to start at zero,
+ * but calls that overlap on the GPU (e.g. on two streams with no ordering
+ * between them) race on it and give undefined results.  The kernels' waits
+ * take the limit of fa_set_wait_timeout_ns() at the time of the call, and an
+ * expired wait is reported by fa_get_last_device_status(), whose status word
+ * (static device memory as well) every entry point shares.
  */
 #define FA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
 fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -290,17 +293,21 @@ const char* fa_status_string(fa_status status);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
- * word.  Every spin-wait inside the kernels is bounded; when one expires the
- * kernel records FA_ERR_TIMEOUT there, drains its own in-flight copies and
+ * word.  Every spin-wait inside the kernels of every entry point (the
+ * allocation-free decode included) is bounded; when one expires the kernel
+ * records FA_ERR_TIMEOUT there, drains its own in-flight copies and
  * tensor-core work, frees its tensor memory and returns (its outputs are then
- * undefined).  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the
- * synchronisation itself failed.
+ * undefined).  The word is static device memory, one per device: reading and
+ * clearing it allocates nothing.  Returns FA_OK, FA_ERR_TIMEOUT, or
+ * FA_ERR_CUDA if the synchronisation itself failed.
  */
 fa_status fa_get_last_device_status(fa_stream_t stream);
 
 /*
  * Sets the limit of every device-side wait, in nanoseconds, for launches made
- * after the call (process-wide; default 2e9 = 2 s; 0 restores the default).
+ * after the call by any entry point (process-wide; default 2e9 = 2 s; 0
+ * restores the default).  The limit travels with each launch as an argument,
+ * so a captured CUDA graph keeps the limit in force when it was captured.
  */
 void fa_set_wait_timeout_ns(unsigned long long ns);
 
