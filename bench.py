@@ -3,8 +3,10 @@
 
 A step is one fa_fwd call (the whole prefill path: tile scheduling, TMA loads,
 S = QK^T, masking, online softmax, lazy O correction, P V, epilogue) over the
-headline workload, the causal MHA prefill B=2, H=16, N=M=2048, d=128, bf16;
-inputs are resident in HBM and L2 is flushed (a 256 MiB write, then a 256 MiB read, so that no dirty line is left to write back) between steps.
+headline workload, the largest single-GPU one: the long causal MHA prefill
+B=1, H=16, N=M=32768, d=128, bf16 (4.4 TFLOP per call); inputs (402 MB) are
+resident in HBM and L2 is flushed (a 256 MiB write, then a 256 MiB read, so
+that no dirty line is left to write back) between steps.
 Each step is timed with CUDA events on the launching stream.  The line also
 carries:
   roofline      the prefill kernel against the measured dense bf16 peak;
@@ -14,7 +16,9 @@ carries:
   decode        split-KV decode (B=2, H=8, M=65536, d=128, chunk 128) in HBM
                 GB/s against the measured copy bandwidth;
   workloads     every workload's time and roofline fraction;
-  cpu_baseline  the fp64 CPU oracle, as it stands, on a bounded sample;
+  cpu_baseline  the fp64 CPU oracle, as it stands, on a bounded sample of
+                the headline workload, and (per_config) of every workload,
+                with the host's core count and CPU model;
   clocks        nvidia-smi samples taken during the timed regions.
 
 --impl reference times the oracle (the only other implementation of the
@@ -40,7 +44,7 @@ if ROOT not in sys.path:
 
 METRIC = ("fwd attention TFLOPS (4·B·H·N·M·d, causal halved) and decode "
           "HBM GB/s, % roofline")
-HEADLINE = "prefill_causal_b2_h16_n2048_bf16"
+HEADLINE = "prefill_causal_h16_n32768_bf16"
 DECODE = "decode_b2_h8_m65536_f16"
 FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 << 20      # GB300 L2; inputs larger than this need no flush between steps
@@ -369,21 +373,26 @@ def bench_e2e_prefill(torch, fa, w, steps, warmup):
 # CPU oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, heads: int):
+def oracle_sample(w, heads: int, rows: int = 0):
     """A bounded sample of workload w for the oracle: batch 0, the first `heads`
-    query heads (with their kv heads), every query row.  Returns a callable that
-    runs it and the sample's algorithmic FLOPs."""
+    query heads (with their kv heads) and either every query row or, with
+    `rows`, the first `rows` of them (with causal masking those rows see only
+    keys 0..rows-1, so the sample is exactly that prefix of the workload).
+    Returns a callable that runs it and the sample's algorithmic FLOPs (the
+    workload's own convention: 4*rows*keys*d per head, halved when causal)."""
     import oracle
     from exact_attention_05_gb300.workloads import bits, workload_inputs
     q, k, v = workload_inputs(w)
     g = w.Hq // w.Hkv
-    kvh = -(-heads // g)
-    qs = bits(q[:1, :, :heads].contiguous())
-    ks = bits(k[:1, :, :kvh].contiguous())
-    vs = bits(v[:1, :, :kvh].contiguous())
     if heads % g:
         raise ValueError("sample must cover whole GQA groups")
-    flops = w.flops / (w.B * w.Hq) * heads
+    kvh = heads // g
+    n = w.N if rows <= 0 else min(rows, w.N)
+    m = min(n, w.M) if (w.causal and n < w.N) else w.M
+    qs = bits(q[:1, :n, :heads].contiguous())
+    ks = bits(k[:1, :m, :kvh].contiguous())
+    vs = bits(v[:1, :m, :kvh].contiguous())
+    flops = 4.0 * heads * n * m * w.d / (2.0 if w.causal else 1.0)
 
     def run():
         oracle.attention(qs, ks, vs, w.dtype, w.causal, w.scale)
@@ -391,7 +400,34 @@ def oracle_sample(w, heads: int):
     return run, flops
 
 
+# Query rows per step of the reference arm: about a second of fp64 work on 16
+# host cores (every row for the workloads smaller than that).
+REFERENCE_ROWS = 16384
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu on Arm hosts, /proc/cpuinfo elsewhere)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w, target_s: float = 12.0):
+    """The oracle on a sample of prefill workload w: whole GQA groups of batch 0,
+    every query row, as many groups as fit in about target_s seconds (at least one)."""
     import oracle
     oracle.build()
     g = w.Hq // w.Hkv
@@ -406,10 +442,45 @@ def cpu_baseline(w, target_s: float = 12.0):
         t0 = time.perf_counter()
         run()
         t1 = time.perf_counter() - t0
+    full = heads == w.Hq and w.B == 1
     return {"value": flops / t1 / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
+            "cpu": cpu_model(), "kind": "oracle", "seconds": t1,
+            "seconds_full_workload": t1 * w.flops / flops,
+            "full_workload_time": "measured" if full else "extrapolated by FLOPs",
             "sample": f"batch 0, query heads 0..{heads - 1} of {w.Hq} (all {w.N} rows), fp64, "
                       f"{t1:.2f} s"}
+
+
+def cpu_baseline_decode(w):
+    """The oracle on a whole 16-bit decode workload (its fp64 pass is short)."""
+    import oracle
+    from exact_attention_05_gb300.workloads import bits, workload_inputs
+    oracle.build()
+    q, k, v = workload_inputs(w)
+    qb, kb, vb = bits(q), bits(k), bits(v)
+    t0 = time.perf_counter()
+    oracle.attention(qb, kb, vb, w.dtype, False, w.scale)
+    t1 = time.perf_counter() - t0
+    return {"value": w.decode_bytes / t1 / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "cpu": cpu_model(), "kind": "oracle", "seconds": t1,
+            "seconds_full_workload": t1, "full_workload_time": "measured",
+            "sample": f"the whole workload (B={w.B}, Hq={w.Hq}, M={w.M}), fp64, {t1:.2f} s"}
+
+
+def cpu_baseline_all(target_s: float = 3.0):
+    """The oracle timed on every 16-bit workload of the table (a bounded sample of
+    each prefill workload, the whole of each decode workload)."""
+    from exact_attention_05_gb300.workloads import WORKLOADS
+    out = {}
+    for name, wl in WORKLOADS.items():
+        if wl.kv != "16bit" or wl.page:
+            continue
+        try:
+            out[name] = cpu_baseline_decode(wl) if wl.kind == "decode" else \
+                cpu_baseline(wl, target_s)
+        except Exception as exc:  # the CPU leg never decides the GPU numbers
+            out[name] = {"value": None, "sample": f"failed: {exc}"}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -421,7 +492,26 @@ def run_reference(args, rank, world):
     oracle.build()
     w = WORKLOADS[args.workload]
     g = w.Hq // w.Hkv
-    run, flops = oracle_sample(w, g)
+    if w.kind == "decode":
+        # one step is the whole decode workload (a short fp64 pass)
+        from exact_attention_05_gb300.workloads import bits, workload_inputs
+        q, k, v = workload_inputs(w)
+        qb, kb, vb = bits(q), bits(k), bits(v)
+
+        def run():
+            oracle.attention(qb, kb, vb, w.dtype, False, w.scale)
+
+        units, per, unit = w.decode_bytes, 1e9, "GB/s"
+        sample = f"the whole workload (B={w.B}, Hq={w.Hq}, M={w.M}) per step, fp64"
+    else:
+        rows = REFERENCE_ROWS
+        run, units = oracle_sample(w, g, rows)
+        per, unit = 1e12, "TFLOP/s"
+        n = min(rows, w.N)
+        what = f"all {w.N} rows" if n == w.N else \
+            f"query rows 0..{n - 1} of {w.N}, the causal prefix" if w.causal else \
+            f"query rows 0..{n - 1} of {w.N}"
+        sample = f"batch 0, query heads 0..{g - 1} of {w.Hq} ({what}) per step, fp64"
     for _ in range(max(0, args.warmup)):
         run()
     times = []
@@ -430,17 +520,16 @@ def run_reference(args, rank, world):
         run()
         times.append(time.perf_counter() - t0)
     mean_s = sum(times) / len(times)
-    value = flops / mean_s / 1e12
-    sample = f"batch 0, query heads 0..{g - 1} of {w.Hq} (all {w.N} rows) per step, fp64"
+    value = units / mean_s / per
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": mean_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
+                         "cpu": cpu_model(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -470,7 +559,7 @@ def workload_config(w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     from exact_attention_05_gb300.workloads import WORKLOADS as _W
@@ -603,12 +692,13 @@ def main(argv=None):
             extras["workloads"] = table
     clk = clocks.summary()
 
-    if rank == 0 and world == 1 and not args.no_extras and not is_decode:
+    if rank == 0 and world == 1 and not args.no_extras:
         try:
-            extras["cpu_baseline"] = cpu_baseline(w)
+            extras["cpu_baseline"] = cpu_baseline_decode(w) if is_decode else cpu_baseline(w)
         except Exception as exc:  # the CPU leg never decides the GPU numbers
-            extras["cpu_baseline"] = {"value": None, "unit": "TFLOP/s", "cores": None,
-                                      "kind": "oracle", "sample": f"failed: {exc}"}
+            extras["cpu_baseline"] = {"value": None, "unit": "GB/s" if is_decode else "TFLOP/s",
+                                      "cores": None, "kind": "oracle", "sample": f"failed: {exc}"}
+        extras["cpu_baseline"]["per_config"] = cpu_baseline_all()
 
     from exact_attention_05_gb300.workloads import DTYPE_NAME
     achieved = units / (mean_ms_max * 1e-3) / per
