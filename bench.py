@@ -483,6 +483,93 @@ def cpu_baseline_all(target_s: float = 3.0):
     return out
 
 
+def latency_breakdown(torch, fa, flush, reps: int = 200):
+    """Where the time of a small call goes, for the two latency-bound workloads
+    (the N=256 prefill and the M=512 decode): the device time of one call after
+    an L2 flush (CUDA events around it, as the table times it); the device time
+    per call of `reps` calls back to back (events around all of them: the
+    launches then overlap the previous kernel's tail); the host time to enqueue
+    one call (the C entry point through the binding, no synchronisation); and
+    the device time per replay of the same calls captured in a CUDA graph."""
+    from exact_attention_05_gb300.workloads import WORKLOADS, workload_inputs
+    out = {}
+    for name in ("prefill_mha_n256_d64_f16", "decode_b1_h8_m512_f16"):
+        w = WORKLOADS[name]
+        if w.kind == "prefill":
+            q, k, v = (t.cuda() for t in workload_inputs(w))
+            o = torch.empty_like(q)
+            lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+
+            def call():
+                fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.N, w.M, w.d, int(w.causal),
+                          w.scale, w.dtype)
+
+            # the same call straight into the C ABI with the pointers and the stream
+            # handle resolved once: the host cost of the library alone
+            lib = fa.load_library()
+            args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B,
+                    w.Hq, w.Hkv, w.N, w.M, w.d, int(w.causal), w.scale, w.dtype,
+                    torch.cuda.current_stream().cuda_stream)
+
+            def abi_call():
+                lib.fa_fwd(*args)
+            launches = 1
+        else:
+            call = decode_call(torch, fa, w)
+            abi_call = None
+            launches = 2
+        single = statistics.median(time_calls(torch, call, 50, 5, flush))
+        for _ in range(10):
+            call()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            call()
+        e.record()
+        torch.cuda.synchronize()
+        chained = s.elapsed_time(e) / reps
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            call()
+        host = (time.perf_counter() - t0) / reps * 1e3
+        torch.cuda.synchronize()
+        host_abi = None
+        if abi_call is not None:
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                abi_call()
+            host_abi = (time.perf_counter() - t0) / reps * 1e3
+            torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            call()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):  # the stream the warm-up call used
+            for _ in range(10):
+                call()
+        graph.replay()
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(reps // 10):
+            graph.replay()
+        e.record()
+        torch.cuda.synchronize()
+        graphed = s.elapsed_time(e) / (reps // 10 * 10)
+        if fa.fa_get_last_device_status() != fa.FA_OK:
+            raise RuntimeError(f"{name}: a device-side wait expired")
+        out[name] = {"launches_per_call": launches, "flushed_single_call_us": single * 1e3,
+                     "back_to_back_us_per_call": chained * 1e3,
+                     "host_enqueue_us_per_call": host * 1e3,
+                     "host_enqueue_abi_us_per_call": None if host_abi is None else host_abi * 1e3,
+                     "cuda_graph_us_per_call": graphed * 1e3}
+    return out
+
+
 def run_reference(args, rank, world):
     """The reference arm: the oracle as it stands on the host cores."""
     if rank != 0:
@@ -567,11 +654,16 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=headline_ok,
                     help="the timed workload (the FP8 and paged decode workloads are timed "
                          "in the per-workload table)")
-    ap.add_argument("--profile", choices=["prefill", "backward", "decode", "decode_single"],
+    ap.add_argument("--profile", choices=["prefill", "backward", "decode", "decode_single",
+                                          "decode_fp8", "decode_paged"],
                     default=None,
                     help="run only --warmup + --steps calls of one operation on --workload "
-                         "(or the long decode workload) and print nothing else: the "
+                         "(or the long decode workload; decode_fp8 and decode_paged take the "
+                         "long e4m3 and paged decode workloads) and print nothing else: the "
                          "command the ncu summaries under profiles/ are taken with")
+    ap.add_argument("--latency", action="store_true",
+                    help="print only the latency breakdown of the two small workloads "
+                         "(flushed single call, back-to-back calls, host enqueue, CUDA graph)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table, decode line and CPU baseline")
     args = ap.parse_args(argv)
@@ -607,10 +699,22 @@ def main(argv=None):
         flush_buf.fill_(flush_ctr[0])
         flush_read.max()
 
+    if args.latency:
+        if rank == 0:
+            print(json.dumps({"latency": latency_breakdown(torch, fa, flush)}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
     if args.profile is not None:
         wp = WORKLOADS[DECODE] if args.profile.startswith("decode") and w.kind != "decode" else w
+        if args.profile == "decode_fp8":
+            wp = WORKLOADS["decode_fp8_b2_h8_m65536_f16"]
+        elif args.profile == "decode_paged":
+            wp = WORKLOADS["decode_paged_b2_h8_m65536_p16_f16"]
         fn = {"prefill": bench_prefill, "backward": bench_backward, "decode": bench_decode,
-              "decode_single": bench_decode_single_launch}[args.profile]
+              "decode_single": bench_decode_single_launch, "decode_fp8": bench_decode,
+              "decode_paged": bench_decode}[args.profile]
         times = fn(torch, fa, wp, args.steps, args.warmup, flush, dist)
         if rank == 0:
             print(f"profile {args.profile} {wp.name}: {len(times)} timed calls, "

@@ -63,7 +63,54 @@ std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
 
 using fa::EncodeTiledFn;
-EncodeTiledFn g_encode = nullptr;
+EncodeTiledFn g_encode_driver = nullptr;  // cuTensorMapEncodeTiled
+
+// Tensor maps already encoded, keyed by every argument of the encode call.
+// A call's tensors are usually the previous call's (the same buffers, one
+// step later), so each map is encoded once and then copied.  Bounded: the
+// cache is emptied when it reaches kMaxCachedMaps entries.
+struct MapKey {
+    uint64_t v[24];
+    bool operator<(const MapKey& o) const { return std::memcmp(v, o.v, sizeof(v)) < 0; }
+};
+constexpr size_t kMaxCachedMaps = 1024;
+std::mutex g_map_mu;
+std::map<MapKey, CUtensorMap> g_maps;
+
+CUresult encode_tiled_cached(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
+                             void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+                             const cuuint32_t* box, const cuuint32_t* estr,
+                             CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                             CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob) {
+    if (rank < 1 || rank > 5) return g_encode_driver(map, dtype, rank, base, dims, strides, box,
+                                                     estr, il, sw, l2, oob);
+    MapKey key{};
+    size_t n = 0;
+    key.v[n++] = reinterpret_cast<uint64_t>(base);
+    key.v[n++] = (uint64_t)dtype | ((uint64_t)rank << 8) | ((uint64_t)il << 16) |
+                 ((uint64_t)sw << 24) | ((uint64_t)l2 << 32) | ((uint64_t)oob << 40);
+    for (cuuint32_t i = 0; i < rank; ++i) key.v[n++] = dims[i];
+    for (cuuint32_t i = 0; i + 1 < rank; ++i) key.v[n++] = strides[i];
+    for (cuuint32_t i = 0; i < rank; ++i) key.v[n++] = ((uint64_t)box[i] << 32) | estr[i];
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *map = it->second;
+            return CUDA_SUCCESS;
+        }
+    }
+    const CUresult r = g_encode_driver(map, dtype, rank, base, dims, strides, box, estr, il, sw,
+                                       l2, oob);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+        g_maps.emplace(key, *map);
+    }
+    return r;
+}
+
+EncodeTiledFn g_encode = nullptr;  // encode_tiled_cached once the driver entry point is known
 
 constexpr uint64_t kMaxElements = 1ull << 39;
 
@@ -116,7 +163,8 @@ fa_status device_state(DeviceState** out) {
                                              &q) != cudaSuccess ||
             q != cudaDriverEntryPointSuccess || fn == nullptr)
             return FA_ERR_CUDA;
-        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        g_encode_driver = reinterpret_cast<EncodeTiledFn>(fn);
+        g_encode = encode_tiled_cached;
     }
     *out = &st;
     return FA_OK;
@@ -230,6 +278,11 @@ int* status_word_current_device() {
 }
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+
+EncodeTiledFn tensor_map_encoder() {
+    DeviceState* st = nullptr;
+    return device_state(&st) == FA_OK ? g_encode : nullptr;
+}
 
 }  // namespace fa
 

@@ -64,8 +64,9 @@ constexpr uint64_t kMaxElements = 1ull << 39;
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // One-time set-up of the current device: architecture check, the device
-// addresses of the static array and of the status word, the tensor-map
-// encoder, the decode kernels' launch attributes.
+// addresses of the static array and of the status word, the library's
+// tensor-map encoder (with its cache of encoded maps), the decode kernels'
+// launch attributes.
 fa_status setup_current_device(DeviceSetup** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -92,14 +93,8 @@ fa_status setup_current_device(DeviceSetup** out) {
             }
         }
         if (s.result == FA_OK && g_encode == nullptr) {
-            cudaDriverEntryPointQueryResult q{};
-            void* fn = nullptr;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                 cudaEnableDefault, &q) != cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || fn == nullptr)
-                s.result = FA_ERR_CUDA;
-            else
-                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+            g_encode = fa::tensor_map_encoder();
+            if (g_encode == nullptr) s.result = FA_ERR_CUDA;
         }
         s.done = true;
     }

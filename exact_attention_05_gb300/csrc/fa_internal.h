@@ -137,6 +137,11 @@ int* status_word_current_device();
 // The current limit of every device-side wait (fa_set_wait_timeout_ns).
 unsigned long long wait_timeout_ns();
 
+// cuTensorMapEncodeTiled behind the library's cache of encoded maps (a map
+// whose arguments were seen before is copied, not encoded again), or nullptr
+// if the current device is not usable.
+EncodeTiledFn tensor_map_encoder();
+
 // Sets a kernel's launch attributes once per device: the largest dynamic
 // shared memory the device allows next to the kernel's static shared memory
 // (so that a launch of any size up to that needs no further set-up), and the
