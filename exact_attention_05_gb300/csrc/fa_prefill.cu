@@ -308,10 +308,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Everything a tile's group of MMAs needs (its P, V_j and the next K
-            // tile) is waited for before the group is issued, so that PV_i(j) and
-            // QK_i(j+1) go to the tensor core back to back.  V_j and K_{j+1} are
-            // checked first: they have normally landed long before, and P is the
-            // one wait that is on the critical path, so nothing follows it.
+            // tile) is complete before the group is issued, so that PV_i(j) and
+            // QK_i(j+1) go to the tensor core back to back.  The group's barriers
+            // are first tested all at once: a barrier test takes ~100 cycles here,
+            // and three of them one after the other (each result deciding whether
+            // to issue the next) left the tensor core idle for ~400 cycles between
+            // two iterations; independent tests overlap.  If one of them is not
+            // complete yet, the bounded waits take over.  V_j and K_{j+1} have
+            // normally landed long before; P is the one on the critical path.
+            auto ready_all = [&](int tile, int j, bool next_k, int nks, uint32_t nkph,
+                                 bool need_vk) -> bool {
+                const bool p_ok = mbar_test_wait(bar(C::B_PFULL + tile), uint32_t(j) & 1u);
+                const bool v_ok = !need_vk || mbar_test_wait(bar_full0 + 8u * vs, vph);
+                const bool k_ok = !need_vk || !next_k || mbar_test_wait(bar_full0 + 8u * nks, nkph);
+                if (p_ok && v_ok && k_ok) return true;
+                // a phase seen complete stays complete until this thread issues the
+                // MMAs that read it, so only the others are waited for
+                return (v_ok || wait_slot(vs, vph)) && (k_ok || wait_slot(nks, nkph)) &&
+                       (p_ok || mbar_wait_spin(bar(C::B_PFULL + tile), uint32_t(j) & 1u, wc,
+                                               FA_SITE_MMA_P));
+            };
             for (int j = 0; ok && j < nt; ++j) {
                 int nks = ks;
                 uint32_t nkph = kph;
@@ -319,8 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool next_k = j + 1 < nt;  // some tile still needs K_{j+1}
                 bool have_vk = false;
                 if (j < nt0) {
-                    if (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph)) ||
-                        !mbar_wait_spin(bar(C::B_PFULL + 0), j & 1, wc, FA_SITE_MMA_P)) {
+                    if (!ready_all(0, j, next_k, nks, nkph, true)) {
                         ok = false;
                         break;
                     }
@@ -330,8 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j + 1 < nt0) qk(0, nks);
                 }
                 if (t1) {
-                    if ((!have_vk && (!wait_slot(vs, vph) || (next_k && !wait_slot(nks, nkph)))) ||
-                        !mbar_wait_spin(bar(C::B_PFULL + 1), j & 1, wc, FA_SITE_MMA_P)) {
+                    if (!ready_all(1, j, next_k, nks, nkph, !have_vk)) {
                         ok = false;
                         break;
                     }
