@@ -90,7 +90,7 @@ struct BwdCfg {
     static constexpr int BAR_OFF = LD_OFF + 2 * LD_BYTES;
     // barriers
     static constexpr int B_KV = 0;       // K_j, V_j landed
-    static constexpr int B_QFULL = 1;    // [2] Q_i, dO_i, LSE/D of a buffer landed
+    static constexpr int B_QFULL = 1;    // [2] Q_i and the LSE/D record of a buffer landed
     static constexpr int B_QFREE = 3;    // [2] the MMAs reading a buffer are done
     static constexpr int B_S = 5;        // S^T in TMEM
     static constexpr int B_DP = 6;       // dP^T in TMEM
@@ -99,9 +99,11 @@ struct BwdCfg {
     static constexpr int B_DQFREE = 9;   // dQ read out of TMEM (256 arrivals)
     static constexpr int B_FINAL = 10;   // every MMA done: dK, dV final
     static constexpr int B_STAGEFULL = 11;  // dQ staged in the tile's Q/dO slots (256 arrivals)
-    static constexpr int B_STAGED = 12;     // [2] the staged dQ of a buffer has been read out
+    static constexpr int B_STAGED = 12;     // [2] the dQ boxes staged in a buffer's Q slot are read out
     static constexpr int B_PT = 14;         // P^T in TMEM (256 arrivals)
-    static constexpr int NBAR = 15;
+    static constexpr int B_DOFULL = 15;     // [2] dO_i of a buffer landed
+    static constexpr int B_STAGED_DO = 17;  // [2] the dQ boxes staged in a buffer's dO slot are read out
+    static constexpr int NBAR = 19;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     // The dynamic shared-memory base is 1 KB aligned (checked at run time), so
     // no alignment slack is allocated: the layout needs all but ~1 KB of the
@@ -242,6 +244,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(C::B_QFULL + x), 1);
             mbar_init(bar(C::B_QFREE + x), 1);
+            mbar_init(bar(C::B_DOFULL + x), 1);
+            mbar_init(bar(C::B_STAGED_DO + x), 1);
         }
         mbar_init(bar(C::B_S), 1);
         mbar_init(bar(C::B_DP), 1);
@@ -283,33 +287,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             // the LSE/D records come from the preprocessing kernel
             grid_dep_wait();
-            int t = 0;
+            // Q_i (with its LSE/D record) and dO_i go into a buffer on barriers of
+            // their own: the buffer's Q slot is refilled as soon as the reducer has
+            // read the dQ boxes staged there, before those in the dO slot, so that
+            // S^T(t) (which needs only Q_i) does not wait for the whole reduction.
+            int t = 0, t_do = 0;  // tiles whose Q (resp. dO) copy was issued
             for (; t < ntile; ++t) {
                 const int buf = t & 1;
-                // the tile two back used this buffer: its MMAs, and its dQ staging in
-                // the dO slot, must be done with it
-                if (t >= 2 && (!mbar_wait(bar(C::B_QFREE + buf), ((t - 2) >> 1) & 1, wc,
-                                          FA_SITE_PRODUCER_SLOT) ||
-                               !mbar_wait(bar(C::B_STAGED + buf), ((t - 2) >> 1) & 1, wc,
-                                          FA_SITE_PRODUCER_SLOT)))
+                const uint32_t ph = ((t - 2) >> 1) & 1;
+                // the tile two back used this buffer: its MMAs, and the dQ staged in
+                // its Q slot, must be done with it
+                if (t >= 2 && (!mbar_wait(bar(C::B_QFREE + buf), ph, wc, FA_SITE_PRODUCER_SLOT) ||
+                               !mbar_wait(bar(C::B_STAGED + buf), ph, wc, FA_SITE_PRODUCER_SLOT)))
                     break;
                 int h, i;
                 tile_of(t, h, i);
                 const uint32_t full = bar(C::B_QFULL + buf);
-                mbar_arrive_expect_tx(full, 2 * C::TILE_BYTES + C::LD_BYTES);
-                for (int s = 0; s < C::NSUB; ++s) {
+                mbar_arrive_expect_tx(full, C::TILE_BYTES + C::LD_BYTES);
+                for (int s = 0; s < C::NSUB; ++s)
                     tma_load_4d(sbase + C::Q_OFF + buf * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q,
                                 s * 64, h, i * C::BM, b, full);
-                    tma_load_4d(sbase + C::DO_OFF + buf * C::TILE_BYTES + s * C::SUB_BYTES, &tm_do,
-                                s * 64, h, i * C::BM, b, full);
-                }
                 bulk_load(sbase + C::LD_OFF + buf * C::LD_BYTES,
                           a.pack + ((size_t(b) * a.Hq + h) * a.n_qtiles + i) * 256, C::LD_BYTES, full);
+                // ... and the dQ staged in its dO slot
+                if (t >= 2 && !mbar_wait(bar(C::B_STAGED_DO + buf), ph, wc, FA_SITE_PRODUCER_SLOT)) {
+                    ++t;  // this tile's Q copy is in flight and must be drained
+                    break;
+                }
+                const uint32_t dfull = bar(C::B_DOFULL + buf);
+                mbar_arrive_expect_tx(dfull, C::TILE_BYTES);
+                for (int s = 0; s < C::NSUB; ++s)
+                    tma_load_4d(sbase + C::DO_OFF + buf * C::TILE_BYTES + s * C::SUB_BYTES, &tm_do,
+                                s * 64, h, i * C::BM, b, dfull);
+                t_do = t + 1;
             }
             // every issued copy must have landed before the CTA may exit
             mbar_drain_wait(bar(C::B_KV), 0, wc, FA_SITE_DRAIN);
             for (int u = t - 2 < 0 ? 0 : t - 2; u < t; ++u)
                 mbar_drain_wait(bar(C::B_QFULL + (u & 1)), (u >> 1) & 1, wc, FA_SITE_DRAIN);
+            for (int u = t_do - 2 < 0 ? 0 : t_do - 2; u < t_do; ++u)
+                mbar_drain_wait(bar(C::B_DOFULL + (u & 1)), (u >> 1) & 1, wc, FA_SITE_DRAIN);
         }
     } else if (warp == 9) {
         // ---------------------------------------------------------- MMA issuer
@@ -353,8 +370,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss(tmem + C::TM_S, k_k + koff(kk), q_k0 + bstep + koff(kk), id_kk,
                            kk > 0 ? 1u : 0u);
                 mma_commit(bar(C::B_S));
-                // dP^T = V dO^T lands where dQ(t-1) is read out from
-                if (t > 0 && !mbar_wait_spin(bar(C::B_DQFREE), (t - 1) & 1, wc, FA_SITE_MMA_P)) {
+                // dP^T = V dO^T lands where dQ(t-1) is read out from, and needs dO_i
+                if ((t > 0 && !mbar_wait_spin(bar(C::B_DQFREE), (t - 1) & 1, wc, FA_SITE_MMA_P)) ||
+                    !mbar_wait_spin(bar(C::B_DOFULL + buf), (t >> 1) & 1, wc, FA_SITE_MMA_Q)) {
                     ok = false;
                     break;
                 }
@@ -404,16 +422,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int buf = t & 1;
                 int h, i;
                 tile_of(t, h, i);
-                for (int k = 0; k < D / 32; ++k)
+                // the boxes in the Q slot first, as one bulk group, then those in the
+                // dO slot; each slot may be refilled (and the CTA may exit) once its
+                // boxes have been read
+                for (int k = 0; k < D / 32; ++k) {
                     tma_reduce_add_4d(&tm_dq,
                                       sbase + (k < C::NSUB ? C::Q_OFF + k * C::SUB_BYTES
                                                            : C::DO_OFF + (k - C::NSUB) * C::SUB_BYTES) +
                                           buf * C::TILE_BYTES,
                                       32 * k, h, i * C::BM, b);
+                    if (k == C::NSUB - 1) tma_store_commit();
+                }
                 tma_store_commit();
-                // once the boxes are read the slots may be refilled (and the CTA may exit)
-                tma_store_wait_all();
+                tma_store_wait_read_1();
                 mbar_arrive(bar(C::B_STAGED + buf));
+                tma_store_wait_all();
+                mbar_arrive(bar(C::B_STAGED_DO + buf));
             }
         }
     } else {

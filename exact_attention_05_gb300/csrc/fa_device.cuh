@@ -282,6 +282,12 @@ __device__ __forceinline__ void tma_store_wait_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Waits until every bulk group of this thread but the most recent one has
+// finished reading its shared-memory source.
+__device__ __forceinline__ void tma_store_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of the same memory.
 __device__ __forceinline__ void fence_async_shared() {
