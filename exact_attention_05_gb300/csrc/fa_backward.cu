@@ -99,7 +99,7 @@ struct BwdCfg {
     static constexpr int B_DQFREE = 9;   // dQ read out of TMEM (256 arrivals)
     static constexpr int B_FINAL = 10;   // every MMA done: dK, dV final
     static constexpr int B_STAGEFULL = 11;  // dQ staged in the tile's Q/dO slots (256 arrivals)
-    static constexpr int B_STAGED = 12;     // [2] the dQ boxes staged in a buffer's Q slot are read out
+    static constexpr int B_STAGED = 12;     // the dQ boxes staged in the dS buffer are read out
     static constexpr int B_PT = 14;         // P^T in TMEM (256 arrivals)
     static constexpr int B_DOFULL = 15;     // [2] dO_i of a buffer landed
     static constexpr int B_STAGED_DO = 17;  // [2] the dQ boxes staged in a buffer's dO slot are read out
@@ -220,6 +220,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
     auto bar = [&](int i) -> uint32_t { return bars + 8u * uint32_t(i); };
+    // Where the fp32 dQ box k (columns [32k, 32k + 32), 128 rows) of a tile in
+    // buffer buf is staged for its bulk reduction: the first NSUB boxes in the dS
+    // buffer (free once the tile's dQ MMA has read dS), the rest in the tile's dO
+    // slot (free once dV and dP have read dO).  The Q slot stays out of it, so
+    // that the next loads of Q never wait for a reduction.
+    auto stage_box = [](int k, int buf) -> uint32_t {
+        return k < C::NSUB ? uint32_t(C::DS_OFF + k * C::SUB_BYTES)
+                           : uint32_t(C::DO_OFF + buf * C::TILE_BYTES + (k - C::NSUB) * C::SUB_BYTES);
+    };
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -256,7 +265,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(C::B_FINAL), 1);
         mbar_init(bar(C::B_STAGEFULL), kComputeThreads);
         mbar_init(bar(C::B_STAGED), 1);
-        mbar_init(bar(C::B_STAGED + 1), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -288,17 +296,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // the LSE/D records come from the preprocessing kernel
             grid_dep_wait();
             // Q_i (with its LSE/D record) and dO_i go into a buffer on barriers of
-            // their own: the buffer's Q slot is refilled as soon as the reducer has
-            // read the dQ boxes staged there, before those in the dO slot, so that
-            // S^T(t) (which needs only Q_i) does not wait for the whole reduction.
+            // their own.  No dQ is staged in the Q slot, so Q_i loads as soon as the
+            // MMAs of the tile two back are done; the dO slot also waits for the
+            // reducer to have read the dQ boxes staged there.
             int t = 0, t_do = 0;  // tiles whose Q (resp. dO) copy was issued
             for (; t < ntile; ++t) {
                 const int buf = t & 1;
                 const uint32_t ph = ((t - 2) >> 1) & 1;
-                // the tile two back used this buffer: its MMAs, and the dQ staged in
-                // its Q slot, must be done with it
-                if (t >= 2 && (!mbar_wait(bar(C::B_QFREE + buf), ph, wc, FA_SITE_PRODUCER_SLOT) ||
-                               !mbar_wait(bar(C::B_STAGED + buf), ph, wc, FA_SITE_PRODUCER_SLOT)))
+                // the tile two back used this buffer: its MMAs must be done with it
+                if (t >= 2 && !mbar_wait(bar(C::B_QFREE + buf), ph, wc, FA_SITE_PRODUCER_SLOT))
                     break;
                 int h, i;
                 tile_of(t, h, i);
@@ -422,20 +428,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int buf = t & 1;
                 int h, i;
                 tile_of(t, h, i);
-                // the boxes in the Q slot first, as one bulk group, then those in the
-                // dO slot; each slot may be refilled (and the CTA may exit) once its
+                // the boxes in the dS buffer first, as one bulk group, then those in
+                // the dO slot; each may be overwritten (and the CTA may exit) once its
                 // boxes have been read
                 for (int k = 0; k < D / 32; ++k) {
-                    tma_reduce_add_4d(&tm_dq,
-                                      sbase + (k < C::NSUB ? C::Q_OFF + k * C::SUB_BYTES
-                                                           : C::DO_OFF + (k - C::NSUB) * C::SUB_BYTES) +
-                                          buf * C::TILE_BYTES,
-                                      32 * k, h, i * C::BM, b);
+                    tma_reduce_add_4d(&tm_dq, sbase + stage_box(k, buf), 32 * k, h, i * C::BM, b);
                     if (k == C::NSUB - 1) tma_store_commit();
                 }
                 tma_store_commit();
                 tma_store_wait_read_1();
-                mbar_arrive(bar(C::B_STAGED + buf));
+                mbar_arrive(bar(C::B_STAGED));
                 tma_store_wait_all();
                 mbar_arrive(bar(C::B_STAGED_DO + buf));
             }
@@ -509,14 +511,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tc_fence_after();
             // ---- dS^T = P^T (dP^T - D): 16-bit into TMEM [128 + 64 wg, +32) and into
-            // smem as dS [query half wg][key row r][64 queries], 128-byte swizzled
+            // smem as dS [query half wg][key row r][64 queries], 128-byte swizzled.  The
+            // smem copy is written last: the dS buffer holds the previous tile's staged
+            // dQ boxes until the reducer has read them.
+            uint32_t dws[2][16];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int qb = 64 * wg + 32 * c;
                 uint32_t dv[32];
                 tmem_ld32(lane_base + C::TM_DP + qb, dv);
                 tmem_wait_ld();
-                uint32_t dw[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
                     const float4 d4 = *reinterpret_cast<const float4*>(dsum + qb + e);
@@ -524,16 +528,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const float d1 = p[32 * c + e + 1] * (__uint_as_float(dv[e + 1]) - d4.y);
                     const float d2 = p[32 * c + e + 2] * (__uint_as_float(dv[e + 2]) - d4.z);
                     const float d3 = p[32 * c + e + 3] * (__uint_as_float(dv[e + 3]) - d4.w);
-                    dw[e / 2] = pack2<T>(d0, d1);
-                    dw[e / 2 + 1] = pack2<T>(d2, d3);
+                    dws[c][e / 2] = pack2<T>(d0, d1);
+                    dws[c][e / 2 + 1] = pack2<T>(d2, d3);
                 }
-                tmem_st16(lane_base + C::TM_DP + 64 * wg + 16 * c, dw);
+                tmem_st16(lane_base + C::TM_DP + 64 * wg + 16 * c, dws[c]);
+            }
+            if (t > 0) {
+                got = mbar_wait(bar(C::B_STAGED), (t - 1) & 1, wc, FA_SITE_SOFTMAX_S);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int cc = 4 * c + u;  // 16-byte chunk (8 queries) within the half
                     const int off = wg * C::SUB_BYTES + r * 128 + ((cc ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4*>(smem + C::DS_OFF + off) =
-                        make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
+                        make_uint4(dws[c][4 * u], dws[c][4 * u + 1], dws[c][4 * u + 2], dws[c][4 * u + 3]);
                 }
             }
             tmem_wait_st();
@@ -561,9 +575,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int x = 0; x < NB; ++x) {
                 const int k = wg * NB + x;
-                uint8_t* box = smem + (k < C::NSUB ? C::Q_OFF + k * C::SUB_BYTES
-                                                   : C::DO_OFF + (k - C::NSUB) * C::SUB_BYTES) +
-                               buf * C::TILE_BYTES;
+                uint8_t* box = smem + stage_box(k, buf);
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     *reinterpret_cast<uint4*>(box + r * 128 + ((u ^ (r & 7)) << 4)) =
