@@ -23,18 +23,18 @@
 //        and dS into shared memory;
 //        dV += P^T dO and dK += dS^T Q take P^T and dS^T straight from TMEM
 //        (A operand in tensor memory); dQ = dS K reads dS from shared memory
-//        (MN-major, i.e. transposed by the descriptor) and lands in the dP^T
-//        columns, query rows on the lanes; the compute warps add it to the fp32
-//        accumulator with vector reductions.
+//        (MN-major, i.e. transposed by the descriptor) and lands in the S^T
+//        columns (P^T is dead by then), query rows on the lanes; the compute
+//        warps stage it for the bulk reductions into the fp32 accumulator.
 //      Q_i, dO_i and the tile's LSE/D record are double-buffered, so the next
 //      tile streams in while the current one is computed.  The tensor core
-//      runs dV(t), dK(t), dQ(t), S^T(t+1) back to back; only dP^T(t+1) waits
-//      for dQ(t) to be read out of TMEM.
-//      TMEM (512 columns): S^T [0,128) (P^T over [0,32) and [64,96)), dP^T
-//      [128,256) (dS^T over [128,160) and [192,224); later dQ over
-//      [128,128+d)), dV [256,256+d), dK [256+d,256+2d).  dQ and S^T(t+1)
-//      overwrite operands that earlier MMAs read: tcgen05 MMAs issued by one
-//      thread execute in issue order.
+//      runs dV(t), then dQ(t) and dK(t) back to back, then S^T(t+1) (which
+//      waits for dQ(t) to be read out of TMEM) and dP^T(t+1).
+//      TMEM (512 columns): S^T [0,128) (P^T over [0,32) and [64,96); later dQ
+//      over [0,d)), dP^T [128,256) (dS^T over [128,160) and [192,224)), dV
+//      [256,256+d), dK [256+d,256+2d).  dQ, dP^T(t+1) and S^T(t+1) overwrite
+//      operands that earlier MMAs read: tcgen05 MMAs issued by one thread
+//      execute in issue order.
 //        warps 0-7 compute; warp 8 TMA producer; warp 9 TMEM allocator and
 //        single-thread MMA issuer; warp 10 issues the dQ bulk reductions.
 //      dQ is read out of TMEM, staged in this tile's Q and dO slots (dead once
@@ -110,7 +110,7 @@ struct BwdCfg {
     // 227 KB a CTA may have.
     static constexpr int SMEM_BYTES = MISC_OFF + 16;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 128, TM_DV = 256, TM_DK = 256 + D;
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 0, TM_DV = 256, TM_DK = 256 + D;
     static_assert(256 + 2 * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -361,35 +361,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t do_m0 = smem_desc(sbase + C::DO_OFF, C::SUB_BYTES, 1024);
             const uint64_t ds_m = smem_desc(sbase + C::DS_OFF, C::SUB_BYTES, 1024);
             const uint64_t k_m = smem_desc(sbase + C::K_OFF, C::SUB_BYTES, 1024);
-            bool ok = mbar_wait_spin(bar(C::B_KV), 0, wc, FA_SITE_MMA_KV);
+            // S^T(tt) = K Q(tt)^T  (M = keys, N = queries, K = d), once Q(tt) has landed
+            auto issue_s = [&](int tt) -> bool {
+                const int b2 = tt & 1;
+                if (!mbar_wait_spin(bar(C::B_QFULL + b2), (tt >> 1) & 1, wc, FA_SITE_MMA_Q))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::TM_S, k_k + koff(kk), q_k0 + (b2 ? kBufStep : 0) + koff(kk),
+                           id_kk, kk > 0 ? 1u : 0u);
+                mma_commit(bar(C::B_S));
+                return true;
+            };
+            // dP^T(tt) = V dO(tt)^T, once dO(tt) has landed; it overwrites dS^T(tt-1),
+            // which dK(tt-1), issued before it, has read by then
+            auto issue_dp = [&](int tt) -> bool {
+                const int b2 = tt & 1;
+                if (!mbar_wait_spin(bar(C::B_DOFULL + b2), (tt >> 1) & 1, wc, FA_SITE_MMA_Q))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::TM_DP, v_k + koff(kk), do_k0 + (b2 ? kBufStep : 0) + koff(kk),
+                           id_kk, kk > 0 ? 1u : 0u);
+                mma_commit(bar(C::B_DP));
+                return true;
+            };
+            bool ok = mbar_wait_spin(bar(C::B_KV), 0, wc, FA_SITE_MMA_KV) && issue_s(0) &&
+                      issue_dp(0);
             for (int t = 0; ok && t < ntile; ++t) {
                 const int buf = t & 1;
                 const uint64_t bstep = buf ? kBufStep : 0;
-                if (!mbar_wait_spin(bar(C::B_QFULL + buf), (t >> 1) & 1, wc, FA_SITE_MMA_Q)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // S^T = K Q^T  (M = keys, N = queries, K = d)
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::TM_S, k_k + koff(kk), q_k0 + bstep + koff(kk), id_kk,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(bar(C::B_S));
-                // dP^T = V dO^T lands where dQ(t-1) is read out from, and needs dO_i
-                if ((t > 0 && !mbar_wait_spin(bar(C::B_DQFREE), (t - 1) & 1, wc, FA_SITE_MMA_P)) ||
-                    !mbar_wait_spin(bar(C::B_DOFULL + buf), (t >> 1) & 1, wc, FA_SITE_MMA_Q)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::TM_DP, v_k + koff(kk), do_k0 + bstep + koff(kk), id_kk,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(bar(C::B_DP));
-                // dV += P^T dO as soon as P^T is there (it overlaps the forming of dS),
-                // then dK += dS^T Q  (M = keys, N = d, K = queries; A in TMEM)
+                // dV += P^T dO as soon as P^T is there (it overlaps the forming of dS)
                 if (!mbar_wait_spin(bar(C::B_PT), t & 1, wc, FA_SITE_MMA_P)) {
                     ok = false;
                     break;
@@ -404,16 +408,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                // dQ = dS K  (M = queries, N = d, K = keys) first, into the S^T columns
+                // (P^T is dead once dV, issued before, has read it), signalled on its own
+                // so that the compute warps read it out while dK runs
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    mma_ss(tmem + C::TM_DQ, ds_m + moff(kk), k_m + moff(kk), id_mm, kk > 0 ? 1u : 0u);
+                mma_commit(bar(C::B_DQ));
+                // dK += dS^T Q  (M = keys, N = d, K = queries; A in TMEM)
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     mma_ts(tmem + C::TM_DK, tmem + C::TM_DP + pcol(kk), q_m0 + bstep + moff(kk), id_ts,
                            (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(C::B_QFREE + buf));  // Q_i, dO_i no longer read
-                // dQ = dS K  (M = queries, N = d, K = keys)
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
-                    mma_ss(tmem + C::TM_DQ, ds_m + moff(kk), k_m + moff(kk), id_mm, kk > 0 ? 1u : 0u);
-                mma_commit(bar(C::B_DQ));
+                if (t + 1 < ntile) {
+                    // S^T(t+1) once dQ(t) has left the S^T columns (the compute warps read
+                    // it out while dK(t) runs), then dP^T(t+1) once dO(t+1) has landed
+                    if (!mbar_wait_spin(bar(C::B_DQFREE), t & 1, wc, FA_SITE_MMA_P) ||
+                        !issue_s(t + 1) || !issue_dp(t + 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
             // every MMA complete: dK, dV are final (and TMEM may be released)
             mma_commit(bar(C::B_FINAL));
