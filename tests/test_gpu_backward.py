@@ -63,6 +63,9 @@ CASES = [
     (1, 2, 2, 130, 1, 64, FP16, False),
     (1, 2, 2, 256, 400, 128, FP16, True),
     (1, 2, 1, 400, 256, 64, BF16, True),
+    # odd GQA group, ragged
+    (1, 6, 2, 333, 333, 128, BF16, True),
+    (1, 3, 1, 200, 260, 64, FP16, False),
 ]
 
 

@@ -33,6 +33,9 @@ CASES = [
     # causal with an even GQA group (two query heads per CTA) and N != M
     (1, 4, 2, 130, 400, 128, FP16, True),
     (2, 8, 2, 400, 131, 64, BF16, True),
+    # causal with an odd GQA group
+    (1, 6, 2, 333, 333, 128, FP16, True),
+    (2, 9, 3, 257, 300, 64, BF16, True),
 ]
 
 
@@ -49,6 +52,10 @@ def test_prefill_parity_small(oracle_mod, case):
 GROUPED = [
     (1, 10, 10, 12900, 12900, 128, BF16, True),
     (1, 32, 16, 8200, 8200, 128, FP16, True),
+    # an odd GQA group (one query head per Q tile pair, three per kv head)
+    (1, 48, 16, 8200, 8200, 128, FP16, True),
+    # non-causal: few query rows against a long key range
+    (1, 4, 4, 300, 36000, 128, BF16, False),
 ]
 
 
