@@ -302,6 +302,7 @@ FA_EXPORT fa_status fa_fwd(const void* q, const void* k, const void* v, void* o,
     if ((s = encode_map(&tv, v, dtype, d, Hkv, M, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
     if ((s = encode_map(&to, o, dtype, d, Hq, N, B, 64, fa::kPrefillTile, true)) != FA_OK) return s;
     fa::PrefillArgs a{};
+    a.o = o;
     a.B = B;
     a.Hq = Hq;
     a.Hkv = Hkv;

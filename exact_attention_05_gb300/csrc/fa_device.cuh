@@ -294,6 +294,77 @@ __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Division by a divisor fixed at launch: q = n / d for 0 <= n < 2^31 as one
+// multiply-high, an add and a shift, with m and s chosen on the host
+// (make_fast_div): s = ceil(log2 d), m = floor(2^32 (2^s - d) / d) + 1, the
+// round-up method of Granlund and Montgomery, "Division by invariant integers
+// using multiplication" (PLDI 1994).  A hardware integer division is a long
+// instruction sequence, and work-item decoding sits on the critical path of a
+// CTA's start.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+    return (__umulhi(n, f.m) + n) >> f.s;
+}
+
+// Brings a 4-D tile into L2 ahead of its load into shared memory (no
+// shared memory, no barrier; out-of-bounds parts are skipped).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// A counter in shared memory that one thread raises and others poll: the
+// release store and acquire load carry the ordering of what the raising
+// thread observed before it.
+__device__ __forceinline__ void st_release_shared(uint32_t addr, int v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_shared(uint32_t addr) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Work stealing among resident CTAs (cluster launch control)
+// ---------------------------------------------------------------------------
+
+// Asks the hardware to cancel the launch of a CTA of this grid that has not
+// started yet.  The 16-byte answer lands at `resp` (16-byte aligned shared
+// memory) and completes 16 transaction bytes on `bar`, whose arrival the
+// caller has armed with mbar_arrive_expect_tx(bar, 16).  After one request
+// has come back empty, no further request may be issued by this CTA.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+        "[%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Reads an answer of clc_try_cancel: the x index of the cancelled CTA, whose
+// work the caller now owns, or -1 if no CTA was left to cancel.
+__device__ __forceinline__ int clc_cancelled_x(uint32_t resp) {
+    uint32_t ok, x = 0xffffffffu;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "+r"(x)
+        : "r"(resp)
+        : "memory");
+    return ok ? (int)x : -1;
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor core
 // ---------------------------------------------------------------------------

@@ -24,11 +24,13 @@ enum FaWaitSite {
     FA_SITE_DECODE_KV = 8,
     FA_SITE_SELFTEST = 9,
     FA_SITE_SMEM_ALIGN = 10,
+    FA_SITE_WORK = 11,   // hand-over of the next work item between the roles of a CTA
 };
 
 namespace fa {
 
 struct PrefillArgs {
+    void* o;               // [B, N, Hq, d], 16-bit
     int B, Hq, Hkv, N, M;
     int causal;
     int n_qtiles;          // ceil(N / 128)

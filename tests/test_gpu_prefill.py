@@ -65,6 +65,25 @@ def test_prefill_parity_l2_groups(oracle_mod, case):
     prefill_case(oracle_mod, *case)
 
 
+# More work items (Q tile pairs) than SMs: resident CTAs take over the items of
+# CTAs that have not started, one after the other, so each of these runs items
+# back to back on one CTA -- including items whose second Q tile lies wholly
+# below the last row (an odd number of row tiles, rows paired), non-causal,
+# d = 64, and causal GQA with two query heads per item and N != M.
+MANY_ITEMS = [
+    (8, 24, 24, 300, 300, 128, BF16, True),
+    (4, 24, 8, 640, 640, 64, FP16, False),
+    (6, 32, 8, 520, 700, 128, FP16, True),
+    (3, 40, 40, 1100, 1100, 64, BF16, True),
+]
+
+
+@pytest.mark.parametrize("case", MANY_ITEMS, ids=lambda c: "B{}_H{}x{}_N{}_M{}_d{}_{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], "causal" if c[7] else "full"))
+def test_prefill_parity_many_items(oracle_mod, case):
+    prefill_case(oracle_mod, *case)
+
+
 @pytest.mark.parametrize("scale", [0.02, 1.0])
 def test_prefill_scale_values(oracle_mod, scale):
     prefill_case(oracle_mod, 1, 2, 2, 300, 300, 128, FP16, True, scale=scale)
