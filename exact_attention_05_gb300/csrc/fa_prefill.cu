@@ -17,9 +17,10 @@
 //     same 128 rows of query heads h and h + 1, which read the same kv head
 //     and so walk the same causal key range.  The grid has one CTA per item,
 //     in dispatch order (L2 groups of heads, heaviest rows first).  One CTA
-//     fits per SM; a CTA that is about to finish its item cancels the launch
-//     of the next CTA that has not started yet (cluster launch control) and
-//     takes over its item, so the CTAs stay resident and one item's start
+//     fits per SM; when the grid has more CTAs than SMs, a CTA that is about
+//     to finish its item cancels the launch of the next CTA that has not
+//     started yet (cluster launch control) and takes over its item, so the
+//     CTAs stay resident and one item's start
 //     overlaps the previous one's end: the next item's Q tiles are brought
 //     into L2 as soon as it is known and loaded as soon as the current Q
 //     tiles are dead, its K/V follow the current ones in the same ring, and
@@ -142,6 +143,7 @@ struct PrefillItem {
 // K/V of few heads.
 struct PrefillSched {
     int pair_heads;  // causal with an even GQA group: tile 1 is the next query head
+    int steal;       // the grid has more CTAs than fit at once: take over pending ones
     int nrow;        // row positions per head unit
     int gbase, grem;
     FastDiv div_nrow, div_g1, div_g0, div_nhu, div_group;  // by nrow, gbase + 1, gbase, units per b, Hq / Hkv
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             int id = blockIdx.x;
-            bool can_steal = true;   // no stealing request has come back empty yet
+            bool can_steal = sc.steal != 0;  // more CTAs than fit at once, and no request came back empty
             bool steal_pending = false;
             uint32_t steal_phase = 0;
             int next = -1;           // the next item, once a stealing request has brought one
@@ -319,16 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         load_q(1, bar(C::B_QFULL1));
                         ++nq1;
                     }
-                    if (l == steal_at && can_steal) {
-                        mbar_arrive_expect_tx(bar(C::B_STEAL), 16);
-                        clc_try_cancel(steal_resp, bar(C::B_STEAL));
-                        steal_pending = true;
-                    } else if (steal_pending && mbar_test_wait(bar(C::B_STEAL), steal_phase)) {
-                        if (!take_steal()) {
-                            ok = false;
-                            break;
-                        }
-                    }
                     const int slot = L % C::NSLOT;
                     if (L >= C::NSLOT) {
                         // The slot's previous load must be consumed: K_m's last reader is
@@ -348,6 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_4d(dst + s * C::SUB_BYTES, map, s * 64, it.kvh, (l >> 1) * C::BN, it.b,
                                     bar(C::B_FULL + slot));
                     ++L;
+                    // after the load, so that the request never delays it
+                    if (l == steal_at && can_steal) {
+                        mbar_arrive_expect_tx(bar(C::B_STEAL), 16);
+                        clc_try_cancel(steal_resp, bar(C::B_STEAL));
+                        steal_pending = true;
+                    } else if (steal_pending && mbar_test_wait(bar(C::B_STEAL), steal_phase)) {
+                        if (!take_steal()) {
+                            ok = false;
+                            break;
+                        }
+                    }
                 }
                 if (!ok) break;
                 s0 += it.nt0;
@@ -872,8 +875,14 @@ cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const
     const double kv_bytes = 2.0 * a.M * D * sizeof(T) * (double)a.B * a.Hkv;
     long long ngroups = (long long)std::ceil(kv_bytes / kL2GroupBytes);
     ngroups = ngroups < 1 ? 1 : (ngroups > nbh ? nbh : ngroups);
+    // one CTA fits per SM; a grid that fits at once has no pending CTAs to take over
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return err;
     PrefillSched sc;
     sc.pair_heads = pair_heads;
+    sc.steal = nblocks > sms ? 1 : 0;
     sc.nrow = pair_heads ? a.n_qtiles : (a.n_qtiles + 1) / 2;
     sc.gbase = (int)(nbh / ngroups);
     sc.grem = (int)(nbh % ngroups);
