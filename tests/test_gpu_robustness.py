@@ -113,3 +113,58 @@ def test_bounded_wait_expires_and_context_survives(oracle_mod):
     o_ref, lse_ref = oracle_mod.attention(bits(q), bits(k), bits(v), FP16, True, 0.1)
     assert_close(o, lse, o_ref, lse_ref, FP16, "after timeout")
     assert np.isfinite(o).all()
+
+
+def test_prefill_many_items_inside_a_captured_cuda_graph():
+    """A prefill grid with more work items than SMs (resident CTAs take over the
+    items of CTAs that have not started) captured into a CUDA graph and replayed
+    with new query values: every replay equals an eager call, bit for bit."""
+    torch = torch_cuda()
+    B, Hq, Hkv, N, M, d = 4, 16, 8, 1024, 1024, 128
+    scale = 1.0 / d ** 0.5
+    q0, k, v = (t.cuda() for t in make_inputs(B, Hq, Hkv, N, M, d, BF16, seed=81))
+    q = q0.clone()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    fa.attention_forward(q, k, v, True, scale, out=o, lse=lse)  # kernel set-up before capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fa.attention_forward(q, k, v, True, scale, out=o, lse=lse)
+    for seed in (82, 83):
+        qn, _, _ = make_inputs(B, Hq, Hkv, N, M, d, BF16, seed=seed)
+        q.copy_(qn.cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        o_ref, lse_ref = fa.attention_forward(q, k, v, True, scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), seed
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+
+
+def test_prefill_grids_on_two_streams_at_once():
+    """Two prefill grids, each with more work items than SMs, enqueued on two
+    streams without ordering between them: CTAs only take over items of their
+    own grid, so each result equals its own call made alone, bit for bit."""
+    torch = torch_cuda()
+    shapes = [(4, 16, 16, 1024, 1024, 128, BF16, True), (3, 24, 8, 700, 900, 64, FP16, False)]
+    inputs, alone = [], []
+    for i, (B, Hq, Hkv, N, M, d, dt, causal) in enumerate(shapes):
+        q, k, v = (t.cuda() for t in make_inputs(B, Hq, Hkv, N, M, d, dt, seed=90 + i))
+        inputs.append((q, k, v, causal, 1.0 / d ** 0.5))
+        o, lse = fa.attention_forward(q, k, v, causal, 1.0 / d ** 0.5)
+        torch.cuda.synchronize()
+        alone.append((o.clone(), lse.clone()))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for rep in range(3):
+        for s, (q, k, v, causal, scale) in zip(streams, inputs):
+            with torch.cuda.stream(s):
+                outs.append(fa.attention_forward(q, k, v, causal, scale, stream=s))
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    for i, (o, lse) in enumerate(outs):
+        o_ref, lse_ref = alone[i % 2]
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), i
