@@ -75,6 +75,12 @@ MANY_ITEMS = [
     (4, 24, 8, 640, 640, 64, FP16, False),
     (6, 32, 8, 520, 700, 128, FP16, True),
     (3, 40, 40, 1100, 1100, 64, BF16, True),
+    # one KV tile per item (N <= 128, two query heads per item): no steady iterations
+    (12, 32, 16, 100, 100, 128, FP16, True),
+    # tile 0 walks one KV tile, tile 1 two (the diagonal), d = 64
+    (2, 100, 100, 200, 200, 64, BF16, True),
+    # every item's second Q tile lies below the last row (N <= 128, rows paired)
+    (4, 48, 48, 100, 300, 128, FP16, False),
 ]
 
 
